@@ -1,0 +1,212 @@
+"""Python binding of the C ABI in ``include/fp8fg.h`` (ctypes over
+``lib/libfp8fg.so``).
+
+Argument marshalling only: every step of the quantization and the GEMM runs
+in the library's CUDA kernels.  PyTorch provides device memory and the
+current stream.  There is no CPU or PyTorch fallback: if the library is
+missing the first call raises.
+
+The functions carry the C names.  They take CUDA torch tensors, allocate any
+output that is not given, call the entry point on the current stream (or
+``stream``) and raise ``Fp8fgError`` on a non-zero status.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+FP8FG_OK = 0
+FP8FG_ERR_INVALID_ARG = 1
+FP8FG_ERR_MISALIGNED = 2
+FP8FG_ERR_UNSUPPORTED_DEVICE = 3
+FP8FG_ERR_CUDA = 4
+FP8FG_ERR_TIMEOUT = 5
+
+FP8FG_OUT_F32 = 0
+FP8FG_OUT_BF16 = 1
+FP8FG_AXIS_COLS = 0
+FP8FG_AXIS_ROWS = 1
+FP8FG_BSCALE_BLOCK128 = 0
+FP8FG_BSCALE_ROW = 1
+
+GROUP = 128
+
+# every entry point the header declares: name -> (restype, argtypes)
+_vp, _i64, _i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+SIGNATURES = {
+    "fp8_quant_act_1x128": (_i32, [_vp, _i64, _i64, _i32, _vp, _vp, _vp]),
+    "fp8_quant_w_128x128": (_i32, [_vp, _i64, _i64, _vp, _vp, _vp, _vp]),
+    "fp8_gemm_blockscaled": (_i32, [_vp, _vp, _vp, _vp, _i32, _i64, _i64, _vp, _i32, _i64, _i64, _i64, _vp]),
+    "fp8_gemm_grouped": (_i32, [_vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i64, _i64, _i64, _vp]),
+    "fp8fg_status_string": (ctypes.c_char_p, [_i32]),
+    "fp8fg_last_device_status": (_i32, [_vp]),
+    "fp8fg_selftest_watchdog": (_i32, [_i64, _vp]),
+}
+
+
+class Fp8fgError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)} (status {status})")
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_missing: bool = False) -> ctypes.CDLL:
+    """Load libfp8fg.so (optionally building it first).  Raises if it is
+    missing: there is no fallback implementation."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = _build.LIB
+    if build_if_missing and (not os.path.exists(path) or _build.is_stale()):
+        _build.build()
+    if not os.path.exists(path):
+        raise RuntimeError(f"CUDA library {path} is not built; run fp8_fine_grained_act_gb300.build.build() "
+                           "(nvcc for sm_103a). There is no CPU fallback.")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load().fp8fg_status_string(int(status)).decode()
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _check(st: int, where: str) -> None:
+    if st != FP8FG_OK:
+        raise Fp8fgError(st, where)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _need(t, dtype, shape, name):
+    if t.dtype != dtype or tuple(t.shape) != tuple(shape) or not t.is_contiguous() or not t.is_cuda:
+        raise ValueError(f"{name}: expected contiguous CUDA {dtype} {tuple(shape)}, got {t.dtype} "
+                         f"{tuple(t.shape)} on {t.device}")
+
+
+# ------------------------------------------------------------ quantizers ---
+
+def fp8_quant_act_1x128(x: torch.Tensor, axis: int = FP8FG_AXIS_COLS, q=None, scales=None, stream=None):
+    """BF16 x[rows, cols] -> (q uint8, scales float32).  axis 0 (1x128 along
+    columns): q[rows, cols], scales[cols/128, rows].  axis 1 (128x1 along
+    rows, transposed output): q[cols, rows], scales[rows/128, cols]."""
+    rows, cols = x.shape
+    if x.dtype != torch.bfloat16 or not x.is_contiguous() or not x.is_cuda:
+        raise ValueError("x must be a contiguous CUDA bfloat16 tensor")
+    if axis == FP8FG_AXIS_COLS:
+        qshape, sshape = (rows, cols), (cols // GROUP, rows)
+    else:
+        qshape, sshape = (cols, rows), (rows // GROUP, cols)
+    if q is None:
+        q = torch.empty(qshape, dtype=torch.uint8, device=x.device)
+    if scales is None:
+        scales = torch.empty(sshape, dtype=torch.float32, device=x.device)
+    _need(q, torch.uint8, qshape, "q")
+    _need(scales, torch.float32, sshape, "scales")
+    st = load().fp8_quant_act_1x128(_ptr(x), rows, cols, int(axis), _ptr(q), _ptr(scales), _stream(stream))
+    _check(st, "fp8_quant_act_1x128")
+    return q, scales
+
+
+def fp8_quant_w_128x128(w: torch.Tensor, transposed: bool = False, q=None, q_t=None, scales=None, stream=None):
+    """FP32 w[rows, cols] -> (q[rows, cols], scales[rows/128, cols/128]) or,
+    with ``transposed``, (q, q_t[cols, rows], scales)."""
+    rows, cols = w.shape
+    if w.dtype != torch.float32 or not w.is_contiguous() or not w.is_cuda:
+        raise ValueError("w must be a contiguous CUDA float32 tensor")
+    if q is None:
+        q = torch.empty((rows, cols), dtype=torch.uint8, device=w.device)
+    if transposed and q_t is None:
+        q_t = torch.empty((cols, rows), dtype=torch.uint8, device=w.device)
+    if scales is None:
+        scales = torch.empty((rows // GROUP, cols // GROUP), dtype=torch.float32, device=w.device)
+    _need(q, torch.uint8, (rows, cols), "q")
+    _need(scales, torch.float32, (rows // GROUP, cols // GROUP), "scales")
+    if q_t is not None:
+        _need(q_t, torch.uint8, (cols, rows), "q_t")
+    st = load().fp8_quant_w_128x128(_ptr(w), rows, cols, _ptr(q), _ptr(q_t), _ptr(scales), _stream(stream))
+    _check(st, "fp8_quant_w_128x128")
+    return (q, q_t, scales) if transposed else (q, scales)
+
+
+# ----------------------------------------------------------------- GEMMs ---
+
+def _out(d, M, N, out_dtype, device):
+    dt = torch.float32 if out_dtype == FP8FG_OUT_F32 else torch.bfloat16
+    if d is None:
+        d = torch.empty((M, N), dtype=dt, device=device)
+    _need(d, dt, (M, N), "d")
+    return d
+
+
+def fp8_gemm_blockscaled(a, sa, b, sb, bscale: int = FP8FG_BSCALE_BLOCK128, sb_strides=None,
+                         out_dtype: int = FP8FG_OUT_BF16, d=None, stream=None):
+    """D[M,N] = A[M,K] . B[N,K]^T with group scales (see include/fp8fg.h).
+    Block mode: sb_strides = (stride_n, stride_k) in elements, default
+    (K/128, 1) for a row-major [N/128, K/128] array."""
+    M, K = a.shape
+    N = b.shape[0]
+    if b.shape[1] != K:
+        raise ValueError("a and b disagree on K")
+    if bscale == FP8FG_BSCALE_BLOCK128:
+        sn, sk = sb_strides if sb_strides is not None else (K // GROUP, 1)
+    else:
+        sn, sk = 0, 0
+    d = _out(d, M, N, out_dtype, a.device)
+    st = load().fp8_gemm_blockscaled(_ptr(a), _ptr(sa), _ptr(b), _ptr(sb), int(bscale), int(sn), int(sk),
+                                     _ptr(d), int(out_dtype), M, N, K, _stream(stream))
+    _check(st, "fp8_gemm_blockscaled")
+    return d
+
+
+def fp8_gemm_grouped(a, sa, b, sb, group_offsets, out_dtype: int = FP8FG_OUT_BF16, d=None, stream=None):
+    """Grouped MoE GEMM: a[M_total, K], b[G, N, K], sb[G, N/128, K/128],
+    group_offsets int32[G+1] on the device."""
+    M, K = a.shape
+    G, N, Kb = b.shape
+    if Kb != K:
+        raise ValueError("a and b disagree on K")
+    if group_offsets.dtype != torch.int32 or not group_offsets.is_cuda or group_offsets.numel() != G + 1:
+        raise ValueError("group_offsets must be a CUDA int32 tensor of G+1 entries")
+    d = _out(d, M, N, out_dtype, a.device)
+    st = load().fp8_gemm_grouped(_ptr(a), _ptr(sa), _ptr(b), _ptr(sb), _ptr(group_offsets), int(G), _ptr(d),
+                                 int(out_dtype), M, N, K, _stream(stream))
+    _check(st, "fp8_gemm_grouped")
+    return d
+
+
+def fp8fg_last_device_status(stream=None) -> int:
+    return int(load().fp8fg_last_device_status(_stream(stream)))
+
+
+def fp8fg_selftest_watchdog(timeout_ns: int, stream=None) -> int:
+    return int(load().fp8fg_selftest_watchdog(int(timeout_ns), _stream(stream)))
+
+
+def fp8fg_status_string(status: int) -> str:
+    return status_string(status)

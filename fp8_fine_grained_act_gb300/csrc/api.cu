@@ -1,0 +1,216 @@
+// api.cu -- the C ABI (include/fp8fg.h): argument validation, device checks,
+// the library-owned device status word, and dispatch to the kernels.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/fp8fg.h"
+#include "kernels.h"
+
+namespace fp8fg {
+namespace {
+
+// Asynchronous errors recorded by kernels (bounded waits, grouped offsets).
+__device__ int g_device_status;
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+    int ok = 0;             // 1 once probed successfully
+    int supported = 0;      // compute capability 10.3
+    int num_sms = 0;
+    int* status_word = nullptr;
+};
+
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Probe the current device once; returns a library status.
+int current_device(DeviceInfo** out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return kErrCuda;
+    std::lock_guard<std::mutex> lock(g_dev_mu);
+    DeviceInfo& d = g_dev[dev];
+    if (!d.ok) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return kErrCuda;
+        d.supported = (major == 10 && minor == 3);
+        d.num_sms = sms;
+        if (d.supported) {
+            void* addr = nullptr;
+            if (cudaGetSymbolAddress(&addr, g_device_status) != cudaSuccess) return kErrCuda;
+            d.status_word = static_cast<int*>(addr);
+        }
+        d.ok = 1;
+    }
+    if (!d.supported) return kErrUnsupported;
+    *out = &d;
+    return kOk;
+}
+
+int from_cuda(cudaError_t e) { return e == cudaSuccess ? kOk : kErrCuda; }
+
+}  // namespace
+}  // namespace fp8fg
+
+using namespace fp8fg;
+
+extern "C" {
+
+int fp8_quant_act_1x128(const void* x_bf16, int64_t rows, int64_t cols, int axis, uint8_t* q, float* scales,
+                        cudaStream_t stream) {
+    if (rows < 0 || cols < 0) return kErrInvalidArg;
+    if (axis != FP8FG_AXIS_COLS && axis != FP8FG_AXIS_ROWS) return kErrInvalidArg;
+    if (axis == FP8FG_AXIS_COLS && cols % 128 != 0) return kErrInvalidArg;
+    if (axis == FP8FG_AXIS_ROWS && (rows % 128 != 0 || cols % 8 != 0)) return kErrInvalidArg;
+    if (rows == 0 || cols == 0) return kOk;
+    if (!x_bf16 || !q || !scales) return kErrInvalidArg;
+    if (rows > (int64_t(1) << 40) / cols) return kErrInvalidArg;
+    if (!aligned16(x_bf16) || !aligned16(q) || !aligned16(scales)) return kErrMisaligned;
+    DeviceInfo* d = nullptr;
+    int st = current_device(&d);
+    if (st != kOk) return st;
+    if (axis == FP8FG_AXIS_COLS) return from_cuda(launch_quant_act_rows(x_bf16, rows, cols, q, scales, d->num_sms, stream));
+    return from_cuda(launch_quant_act_cols(x_bf16, rows, cols, q, scales, d->num_sms, stream));
+}
+
+int fp8_quant_w_128x128(const float* w, int64_t rows, int64_t cols, uint8_t* q, uint8_t* q_t, float* scales,
+                        cudaStream_t stream) {
+    if (rows < 0 || cols < 0 || rows % 128 != 0 || cols % 128 != 0) return kErrInvalidArg;
+    if (rows == 0 || cols == 0) return kOk;
+    if (!w || !q || !scales) return kErrInvalidArg;
+    if (rows > (int64_t(1) << 40) / cols) return kErrInvalidArg;
+    if (!aligned16(w) || !aligned16(q) || !aligned16(scales) || (q_t && !aligned16(q_t))) return kErrMisaligned;
+    DeviceInfo* d = nullptr;
+    int st = current_device(&d);
+    if (st != kOk) return st;
+    return from_cuda(launch_quant_w(w, rows, cols, q, q_t, scales, d->num_sms, stream));
+}
+
+static int gemm_common(const GemmArgs& a, cudaStream_t stream) {
+    DeviceInfo* d = nullptr;
+    int st = current_device(&d);
+    if (st != kOk) return st;
+    if (a.K == 0) {
+        const size_t elt = a.out_bf16 ? 2 : 4;
+        return from_cuda(cudaMemsetAsync(a.d, 0, static_cast<size_t>(a.M) * a.N * elt, stream));
+    }
+    cudaError_t ce = cudaSuccess;
+    return launch_gemm(a, d->num_sms, d->status_word, stream, &ce);
+}
+
+// Shape rules shared by the dense and grouped GEMMs.  TMA addresses rows of
+// up to 2^32 elements per dimension; the limits below keep every index and
+// byte count far inside int64 and the tensor-map ranges.
+static int check_gemm_shape(int64_t M, int64_t N, int64_t K, int out_dtype) {
+    if (M < 0 || N < 0 || K < 0) return kErrInvalidArg;
+    if (M % 128 != 0 || N % 128 != 0 || K % 128 != 0) return kErrInvalidArg;
+    if (out_dtype != FP8FG_OUT_F32 && out_dtype != FP8FG_OUT_BF16) return kErrInvalidArg;
+    const int64_t lim = int64_t(1) << 31;
+    if (M > lim || N > lim || K > lim) return kErrInvalidArg;
+    // output tiles of 128 x 256 are numbered with 32-bit integers
+    if ((M / 128) * ((N + 255) / 256) >= lim) return kErrInvalidArg;
+    return kOk;
+}
+
+int fp8_gemm_blockscaled(const uint8_t* a, const float* sa, const uint8_t* b, const float* sb, int bscale,
+                         int64_t sb_stride_n, int64_t sb_stride_k, void* d, int out_dtype, int64_t M, int64_t N,
+                         int64_t K, cudaStream_t stream) {
+    int st = check_gemm_shape(M, N, K, out_dtype);
+    if (st != kOk) return st;
+    if (bscale != FP8FG_BSCALE_BLOCK128 && bscale != FP8FG_BSCALE_ROW) return kErrInvalidArg;
+    if (bscale == FP8FG_BSCALE_BLOCK128 && (sb_stride_n < 0 || sb_stride_k < 0)) return kErrInvalidArg;
+    if (M == 0 || N == 0) return kOk;
+    if (!d) return kErrInvalidArg;
+    if (K > 0 && (!a || !sa || !b || !sb)) return kErrInvalidArg;
+    if (!aligned16(d) || (K > 0 && (!aligned16(a) || !aligned16(sa) || !aligned16(b) || !aligned16(sb))))
+        return kErrMisaligned;
+    GemmArgs g{};
+    g.a = a;
+    g.sa = sa;
+    g.b = b;
+    g.sb = sb;
+    g.bscale = bscale;
+    g.sb_stride_n = sb_stride_n;
+    g.sb_stride_k = sb_stride_k;
+    g.d = d;
+    g.out_bf16 = out_dtype == FP8FG_OUT_BF16;
+    g.M = M;
+    g.N = N;
+    g.K = K;
+    g.offsets = nullptr;
+    g.G = 0;
+    return gemm_common(g, stream);
+}
+
+int fp8_gemm_grouped(const uint8_t* a, const float* sa, const uint8_t* b, const float* sb,
+                     const int32_t* group_offsets, int G, void* d, int out_dtype, int64_t M_total, int64_t N,
+                     int64_t K, cudaStream_t stream) {
+    int st = check_gemm_shape(M_total, N, K, out_dtype);
+    if (st != kOk) return st;
+    if (G < 1 || G > 4096) return kErrInvalidArg;
+    if (!group_offsets) return kErrInvalidArg;
+    if (M_total == 0 || N == 0) return kOk;
+    if (!d) return kErrInvalidArg;
+    if (K > 0 && (!a || !sa || !b || !sb)) return kErrInvalidArg;
+    if (!aligned16(d) || (K > 0 && (!aligned16(a) || !aligned16(sa) || !aligned16(b) || !aligned16(sb))) ||
+        (reinterpret_cast<uintptr_t>(group_offsets) & 3u))
+        return kErrMisaligned;
+    GemmArgs g{};
+    g.a = a;
+    g.sa = sa;
+    g.b = b;
+    g.sb = sb;
+    g.bscale = FP8FG_BSCALE_BLOCK128;
+    g.sb_stride_n = K / 128;
+    g.sb_stride_k = 1;
+    g.d = d;
+    g.out_bf16 = out_dtype == FP8FG_OUT_BF16;
+    g.M = M_total;
+    g.N = N;
+    g.K = K;
+    g.offsets = group_offsets;
+    g.G = G;
+    return gemm_common(g, stream);
+}
+
+const char* fp8fg_status_string(int status) {
+    switch (status) {
+        case FP8FG_OK: return "FP8FG_OK";
+        case FP8FG_ERR_INVALID_ARG: return "FP8FG_ERR_INVALID_ARG: invalid argument (null pointer, enum or shape)";
+        case FP8FG_ERR_MISALIGNED: return "FP8FG_ERR_MISALIGNED: a pointer is not 16-byte aligned";
+        case FP8FG_ERR_UNSUPPORTED_DEVICE: return "FP8FG_ERR_UNSUPPORTED_DEVICE: the current device is not sm_103";
+        case FP8FG_ERR_CUDA: return "FP8FG_ERR_CUDA: a CUDA call or a kernel launch failed";
+        case FP8FG_ERR_TIMEOUT: return "FP8FG_ERR_TIMEOUT: a bounded device wait ran out";
+        default: return "FP8FG: unknown status";
+    }
+}
+
+int fp8fg_last_device_status(cudaStream_t stream) {
+    DeviceInfo* d = nullptr;
+    int st = current_device(&d);
+    if (st != kOk) return st;
+    int value = 0;
+    const int zero = 0;
+    if (cudaMemcpyAsync(&value, d->status_word, sizeof(int), cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
+        cudaMemcpyAsync(d->status_word, &zero, sizeof(int), cudaMemcpyHostToDevice, stream) != cudaSuccess ||
+        cudaStreamSynchronize(stream) != cudaSuccess)
+        return kErrCuda;
+    return value;
+}
+
+int fp8fg_selftest_watchdog(int64_t timeout_ns, cudaStream_t stream) {
+    if (timeout_ns < 1 || timeout_ns > 1000000000) return kErrInvalidArg;
+    DeviceInfo* d = nullptr;
+    int st = current_device(&d);
+    if (st != kOk) return st;
+    return from_cuda(launch_watchdog_selftest(static_cast<uint64_t>(timeout_ns), d->status_word, stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,526 @@
+// gemm.cu -- block-scaled FP8 GEMM on sm_103a tensor cores (tcgen05 + TMEM).
+//
+// D[M, N] = A[M, K] . B[N, K]^T, both operands K-major E4M3 with one FP32
+// scale per 128-wide K chunk (per row of A; per 128x128 block or per row of
+// B).  For every K chunk c the tensor cores accumulate
+//     P = sum_{k in chunk c} a[i, k] b[j, k]        (FP32, in TMEM)
+// and the epilogue warps promote it into FP32 registers:
+//     acc[i, j] += P[i, j] * (sa[c, i] * sb(j, c)).
+// Sources: "DeepSeek FP8 Training" (arcalunar.github.io), forward pipeline
+// steps 3-4 (tile-based FP8 GEMM, FP32 accumulation, BF16 output) and the
+// Wgrad / Dgrad pipelines (FP32 and BF16 outputs); DeepSeek-V3 FP8 post
+// (innerforce.co.kr), increased-precision accumulation paragraph (the FP8
+// MMA's own accumulation is limited, so partial sums are promoted to FP32
+// with the dequantization folded in); "Unified E4M3 format in DeepSeek-V3"
+// (codingmall.com), Enhanced Numerical Stability (promotion to FP32 registers
+// at fixed intervals; the interval here is one 128-wide group).
+//
+// Kernel structure (one persistent CTA per SM, 12 warps in 3 warpgroups;
+// warpgroup 0 gives registers to the epilogue warpgroups with setmaxnreg):
+//   warp 0      TMA producer: A tile [128 x 128 B] and B tile [256 x 128 B]
+//               per K chunk into a 4-stage shared-memory ring (128-byte
+//               swizzle), plus the chunk's A scales (and per-row B scales)
+//               into an 8-slot scale ring, all completing on mbarriers;
+//   warp 1      MMA issuer: 4 x tcgen05.mma.kind::f8f6f4 (K = 32 each) per
+//               chunk into one of two 256-column TMEM buffers, then commits
+//               to the stage's "empty" barrier and the buffer's "full" one;
+//   warps 2-3   idle;
+//   warps 4-11  epilogue: tcgen05.ld the chunk's partial sums, release the
+//               TMEM buffer, scale-and-add into 128 FP32 registers per
+//               thread (one row, 128 columns), and after the last chunk
+//               convert and store.
+// The MMA of chunk c+1 runs while the epilogue promotes chunk c.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace fp8fg {
+namespace {
+
+constexpr int BM = 128;   // rows of A per tile (TMEM lanes)
+constexpr int BN = 256;   // rows of B per tile (TMEM columns per buffer)
+constexpr int BK = 128;   // one quantization group along K
+constexpr int MMA_K = 32; // K per tcgen05.mma for 8-bit operands
+constexpr int STAGES = 4;
+constexpr int SLOTS = 8;
+constexpr int EPI_WARPS = 8;
+constexpr int THREADS = 128 + 32 * EPI_WARPS;
+// registers per thread: 168 at launch (384 x 168 = 64512); after the split
+// warpgroup 0 keeps 64 and the two epilogue warpgroups take 216 each
+// (128 x 64 + 256 x 216 = 63488, within the launch total).
+constexpr int REGS_LOW = 64, REGS_HIGH = 216;
+constexpr uint32_t TMEM_COLS = 2 * BN;
+constexpr uint32_t A_BYTES = BM * BK;
+constexpr uint32_t B_BYTES = BN * BK;
+
+struct __align__(1024) Smem {
+    uint8_t a[STAGES][A_BYTES];
+    uint8_t b[STAGES][B_BYTES];
+    float sa[SLOTS][BM];
+    float sb[SLOTS][BN];
+    uint64_t full[STAGES];
+    uint64_t empty[STAGES];
+    uint64_t tfull[2];
+    uint64_t tempty[2];
+    uint64_t sfull[SLOTS];
+    uint64_t sempty[SLOTS];
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort_flag;
+    int bad_offsets;
+};
+
+constexpr size_t kSmemBytes = sizeof(Smem) + 1024;  // + alignment slack of the dynamic buffer
+
+struct Params {
+    const float* sa;
+    const float* sb;
+    int64_t sb_stride_n;
+    int64_t sb_stride_k;
+    int64_t sb_group_stride;  // grouped: elements between consecutive experts' scale arrays
+    int bscale;
+    void* d;
+    int out_bf16;
+    int64_t M, N, K;
+    const int32_t* offsets;
+    int G;
+    int m_fastest;
+    int* status;
+    uint64_t limit_ns;
+};
+
+// Shared-memory matrix descriptor of a K-major tile written by TMA with the
+// 128-byte swizzle: rows of 128 bytes, 8-row groups 1024 bytes apart.
+//   bits  0-13  start address >> 4
+//   bits 16-29  leading-dimension byte offset >> 4 (unused for this layout: 1)
+//   bits 32-45  stride-dimension byte offset >> 4 (1024 B between 8-row groups)
+//   bits 46-48  fixed 0b001
+//   bits 61-63  swizzle mode (2 = 128-byte swizzle)
+FP8FG_DEV uint64_t smem_desc_sw128(uint32_t saddr) {
+    uint64_t d = static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>(1) << 16;
+    d |= static_cast<uint64_t>(1024 >> 4) << 32;
+    d |= static_cast<uint64_t>(1) << 46;
+    d |= static_cast<uint64_t>(2) << 61;
+    return d;
+}
+
+// Instruction descriptor, kind::f8f6f4: D = F32 (bits 4-5 = 1), A = B = E4M3
+// (bits 7-9, 10-12 = 0), both K-major (bits 15, 16 = 0), N >> 3 at bits
+// 17-22, M >> 4 at bits 24-28.
+constexpr uint32_t kIdesc = (1u << 4) | (static_cast<uint32_t>(BN >> 3) << 17) | (static_cast<uint32_t>(BM >> 4) << 24);
+
+// Tile t -> origin (m0, n0).  Tile counts fit in 32 bits (checked on the
+// host), so the divisions stay 32-bit and inline.
+FP8FG_DEV void tile_origin(int64_t t, int64_t m_tiles, int64_t n_tiles, int m_fastest, int64_t& m0, int64_t& n0) {
+    const uint32_t tt = static_cast<uint32_t>(t);
+    if (m_fastest) {
+        const uint32_t mt = static_cast<uint32_t>(m_tiles);
+        const uint32_t q = tt / mt;
+        m0 = static_cast<int64_t>(tt - q * mt) * BM;
+        n0 = static_cast<int64_t>(q) * BN;
+    } else {
+        const uint32_t nt = static_cast<uint32_t>(n_tiles);
+        const uint32_t q = tt / nt;
+        m0 = static_cast<int64_t>(q) * BM;
+        n0 = static_cast<int64_t>(tt - q * nt) * BN;
+    }
+}
+
+// Expert owning row m0: the g with offsets[g] <= m0 < offsets[g+1].
+FP8FG_DEV int expert_of(const int32_t* offsets, int G, int64_t m0) {
+    int lo = 0, hi = G;
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (static_cast<int64_t>(__ldg(offsets + mid)) <= m0)
+            lo = mid;
+        else
+            hi = mid;
+    }
+    return lo;
+}
+
+// Wait that ignores the abort flag (tear-down): bounded by `limit_ns`.
+FP8FG_DEV bool wait_plain(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity))
+        if (globaltimer_ns() - t0 > limit_ns) return false;
+    return true;
+}
+
+FP8FG_DEV uint32_t pack_bf16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// ------------------------------------------------------------ producer ---
+// kRowB: B scales per row of B per K chunk (1) or per 128x128 block (0).
+template <int kRowB>
+FP8FG_DEV void run_producer(Smem& sm, const CUtensorMap* tmap_a, const CUtensorMap* tmap_b, const Params& p,
+                            int64_t m_tiles, int64_t n_tiles, int64_t kb) {
+    volatile int* abort_flag = &sm.abort_flag;
+    uint32_t g_ab = 0, g_sc = 0;  // chunks whose operand / scale copies were issued
+    const int64_t num_tiles = m_tiles * n_tiles;
+    bool ok = true;
+    for (int64_t t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
+        int64_t m0, n0;
+        tile_origin(t, m_tiles, n_tiles, p.m_fastest, m0, n0);
+        const int e = p.offsets ? expert_of(p.offsets, p.G, m0) : 0;
+        uint32_t sc_bytes = BM * 4;
+        if (kRowB) sc_bytes += static_cast<uint32_t>(min(static_cast<int64_t>(BN), p.N - n0) * 4);
+        for (int64_t c = 0; c < kb; ++c) {
+            const uint32_t s = g_ab % STAGES, ph = (g_ab / STAGES) & 1;
+            if (!mbar_wait_bounded(smem_u32(&sm.empty[s]), ph ^ 1, abort_flag, p.status, p.limit_ns, kErrTimeout)) {
+                ok = false;
+                break;
+            }
+            const uint32_t fb = smem_u32(&sm.full[s]);
+            mbar_arrive_expect_tx(fb, A_BYTES + B_BYTES);
+            tma_load_2d(smem_u32(sm.a[s]), tmap_a, static_cast<int32_t>(c * BK), static_cast<int32_t>(m0), fb);
+            if (p.offsets)
+                tma_load_3d(smem_u32(sm.b[s]), tmap_b, static_cast<int32_t>(c * BK), static_cast<int32_t>(n0), e, fb);
+            else
+                tma_load_2d(smem_u32(sm.b[s]), tmap_b, static_cast<int32_t>(c * BK), static_cast<int32_t>(n0), fb);
+            ++g_ab;
+            const uint32_t sl = g_sc % SLOTS, sph = (g_sc / SLOTS) & 1;
+            if (!mbar_wait_bounded(smem_u32(&sm.sempty[sl]), sph ^ 1, abort_flag, p.status, p.limit_ns,
+                                   kErrTimeout)) {
+                ok = false;
+                break;
+            }
+            const uint32_t sfb = smem_u32(&sm.sfull[sl]);
+            mbar_arrive_expect_tx(sfb, sc_bytes);
+            bulk_load(smem_u32(sm.sa[sl]), p.sa + c * p.M + m0, BM * 4, sfb);
+            if (kRowB) bulk_load(smem_u32(sm.sb[sl]), p.sb + c * p.N + n0, sc_bytes - BM * 4, sfb);
+            ++g_sc;
+        }
+    }
+    if (!ok) {
+        // abort: let the copies already issued land before the CTA exits
+        for (uint32_t s = 0; s < STAGES && s < g_ab; ++s) {
+            const uint32_t last = s + STAGES * ((g_ab - 1 - s) / STAGES);
+            wait_plain(smem_u32(&sm.full[s]), (last / STAGES) & 1, 10000000ull);
+        }
+        for (uint32_t s = 0; s < SLOTS && s < g_sc; ++s) {
+            const uint32_t last = s + SLOTS * ((g_sc - 1 - s) / SLOTS);
+            wait_plain(smem_u32(&sm.sfull[s]), (last / SLOTS) & 1, 10000000ull);
+        }
+    }
+}
+
+// ----------------------------------------------------------------- MMA ---
+FP8FG_DEV void run_mma(Smem& sm, uint32_t tmem_base, const Params& p, int64_t m_tiles, int64_t n_tiles, int64_t kb) {
+    volatile int* abort_flag = &sm.abort_flag;
+    uint32_t g = 0;
+    const int64_t num_tiles = m_tiles * n_tiles;
+    bool ok = true;
+    for (int64_t t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
+        for (int64_t c = 0; c < kb; ++c, ++g) {
+            const uint32_t s = g % STAGES, ph = (g / STAGES) & 1;
+            const uint32_t buf = g & 1, tph = (g >> 1) & 1;
+            if (!mbar_wait_bounded(smem_u32(&sm.tempty[buf]), tph ^ 1, abort_flag, p.status, p.limit_ns,
+                                   kErrTimeout) ||
+                !mbar_wait_bounded(smem_u32(&sm.full[s]), ph, abort_flag, p.status, p.limit_ns, kErrTimeout)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t d_tmem = tmem_base + buf * BN;
+            const uint64_t adesc = smem_desc_sw128(smem_u32(sm.a[s]));
+            const uint64_t bdesc = smem_desc_sw128(smem_u32(sm.b[s]));
+#pragma unroll
+            for (int kk = 0; kk < BK / MMA_K; ++kk) {
+                // advance 32 bytes along K inside the 128-byte swizzle atom
+                const uint64_t koff = static_cast<uint64_t>((kk * MMA_K) >> 4);
+                mma_f8f6f4(d_tmem, adesc + koff, bdesc + koff, kIdesc, kk > 0 ? 1u : 0u);
+            }
+            mma_commit(smem_u32(&sm.empty[s]));
+            mma_commit(smem_u32(&sm.tfull[buf]));
+        }
+    }
+    // every MMA issued by this thread has finished before TMEM is released
+    mma_commit(smem_u32(&sm.drain));
+    wait_plain(smem_u32(&sm.drain), 0, 100000000ull);
+}
+
+// ------------------------------------------------------------ epilogue ---
+template <int kRowB>
+FP8FG_DEV void run_epilogue(Smem& sm, uint32_t tmem_base, const Params& p, int64_t m_tiles, int64_t n_tiles,
+                            int64_t kb, int warp, int lane) {
+    volatile int* abort_flag = &sm.abort_flag;
+    const int quad = warp & 3;          // TMEM lanes this warp may read: 32*quad .. 32*quad+31
+    const int half = (warp - 4) >> 2;   // columns 128*half .. 128*half+127 of the tile
+    const int row = quad * 32 + lane;   // tile row owned by this thread
+    const uint32_t t_lane = static_cast<uint32_t>(quad * 32) << 16;
+    const int64_t num_tiles = m_tiles * n_tiles;
+    uint32_t g = 0;
+    for (int64_t t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+        int64_t m0, n0;
+        tile_origin(t, m_tiles, n_tiles, p.m_fastest, m0, n0);
+        const int64_t col0 = n0 + 128 * half;
+        const bool active = col0 < p.N;
+        // block-mode B scales: lane l holds the scale of chunk 32*batch + l
+        const float* sbp = p.sb;
+        if (!kRowB) {
+            const int e = p.offsets ? expert_of(p.offsets, p.G, m0) : 0;
+            sbp = p.sb + e * p.sb_group_stride + (col0 / 128) * p.sb_stride_n;
+        }
+        float sb_cur = 0.0f, sb_nxt = 0.0f;
+        if (!kRowB && active) {
+            if (lane < kb) sb_cur = __ldg(sbp + lane * p.sb_stride_k);
+            if (lane + 32 < kb) sb_nxt = __ldg(sbp + (lane + 32) * p.sb_stride_k);
+        }
+        float acc[128];
+#pragma unroll
+        for (int j = 0; j < 128; ++j) acc[j] = 0.0f;
+        for (int64_t c = 0; c < kb; ++c, ++g) {
+            const uint32_t buf = g & 1, tph = (g >> 1) & 1;
+            const uint32_t sl = g % SLOTS, sph = (g / SLOTS) & 1;
+            if (!kRowB && c > 0 && (c & 31) == 0) {
+                sb_cur = sb_nxt;
+                sb_nxt = (active && c + 32 + lane < kb) ? __ldg(sbp + (c + 32 + lane) * p.sb_stride_k) : 0.0f;
+            }
+            // every lane waits (each gets the barrier's acquire); the verdict
+            // is made warp-uniform before any warp-collective instruction
+            bool ok = mbar_wait_bounded(smem_u32(&sm.tfull[buf]), tph, abort_flag, p.status, p.limit_ns, kErrTimeout);
+            ok = ok && mbar_wait_bounded(smem_u32(&sm.sfull[sl]), sph, abort_flag, p.status, p.limit_ns, kErrTimeout);
+            if (!__all_sync(0xffffffffu, ok)) return;
+            tc_fence_after();
+            const float sa_i = sm.sa[sl][row];
+            const float sbv = __shfl_sync(0xffffffffu, sb_cur, static_cast<int>(c & 31));
+            if (active) {
+                const uint32_t taddr = tmem_base + t_lane + buf * BN + 128 * half;
+                if (!kRowB) {
+                    const float scale = sa_i * sbv;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        uint32_t r[32];
+                        tmem_ld_32x32b_x32(taddr + 32 * j, r);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int k = 0; k < 32; ++k) acc[32 * j + k] = fmaf(__uint_as_float(r[k]), scale, acc[32 * j + k]);
+                    }
+                } else {
+                    const float* sbrow = sm.sb[sl] + 128 * half;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        uint32_t r[32];
+                        tmem_ld_32x32b_x32(taddr + 32 * j, r);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int k = 0; k < 32; ++k)
+                            acc[32 * j + k] = fmaf(__uint_as_float(r[k]) * sbrow[32 * j + k], sa_i, acc[32 * j + k]);
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(smem_u32(&sm.tempty[buf]));
+                mbar_arrive(smem_u32(&sm.sempty[sl]));
+            }
+        }
+        if (!active) continue;
+        if (p.out_bf16) {
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.d) + (m0 + row) * p.N + col0);
+#pragma unroll
+            for (int v = 0; v < 16; ++v) {
+                uint4 o;
+                o.x = pack_bf16x2(acc[8 * v + 0], acc[8 * v + 1]);
+                o.y = pack_bf16x2(acc[8 * v + 2], acc[8 * v + 3]);
+                o.z = pack_bf16x2(acc[8 * v + 4], acc[8 * v + 5]);
+                o.w = pack_bf16x2(acc[8 * v + 6], acc[8 * v + 7]);
+                dst[v] = o;
+            }
+        } else {
+            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.d) + (m0 + row) * p.N + col0);
+#pragma unroll
+            for (int v = 0; v < 32; ++v)
+                dst[v] = make_float4(acc[4 * v + 0], acc[4 * v + 1], acc[4 * v + 2], acc[4 * v + 3]);
+        }
+    }
+}
+
+template <int kRowB>
+__global__ void __launch_bounds__(THREADS, 1)
+    gemm_blockscaled_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+                            const Params p) {
+    extern __shared__ uint8_t smem_raw[];
+    Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t m_tiles = p.M / BM, n_tiles = (p.N + BN - 1) / BN, kb = p.K / BK;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(smem_u32(&sm.full[s]), 1);
+            mbar_init(smem_u32(&sm.empty[s]), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(&sm.tfull[b]), 1);
+            mbar_init(smem_u32(&sm.tempty[b]), EPI_WARPS);
+        }
+        for (int s = 0; s < SLOTS; ++s) {
+            mbar_init(smem_u32(&sm.sfull[s]), 1);
+            mbar_init(smem_u32(&sm.sempty[s]), EPI_WARPS);
+        }
+        mbar_init(smem_u32(&sm.drain), 1);
+        sm.abort_flag = 0;
+        sm.bad_offsets = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tensormap(&tmap_a);
+        prefetch_tensormap(&tmap_b);
+    }
+    if (warp == 1) tmem_alloc(smem_u32(&sm.tmem_base), TMEM_COLS);
+    int bad = 0;
+    if (p.offsets) {
+        // grouped offsets must start at 0, end at M, be non-decreasing and
+        // multiples of 128; otherwise nothing is computed or written
+        for (int g = threadIdx.x; g <= p.G; g += THREADS) {
+            const int64_t o = __ldg(p.offsets + g);
+            if (o < 0 || o > p.M || (o % BM) != 0) bad = 1;
+            if (g == 0 && o != 0) bad = 1;
+            if (g == p.G && o != p.M) bad = 1;
+            if (g > 0 && static_cast<int64_t>(__ldg(p.offsets + g - 1)) > o) bad = 1;
+        }
+    }
+    tc_fence_before();
+    bad = __syncthreads_or(bad);
+    tc_fence_after();
+    const uint32_t tmem_base = sm.tmem_base;
+    if (bad) {
+        if (blockIdx.x == 0 && threadIdx.x == 0) atomicCAS(p.status, 0, kErrInvalidArg);
+    } else if (warp < 4) {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(REGS_LOW));
+        if (warp == 0 && lane == 0) run_producer<kRowB>(sm, &tmap_a, &tmap_b, p, m_tiles, n_tiles, kb);
+        if (warp == 1 && lane == 0) run_mma(sm, tmem_base, p, m_tiles, n_tiles, kb);
+    } else {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(REGS_HIGH));
+        run_epilogue<kRowB>(sm, tmem_base, p, m_tiles, n_tiles, kb, warp, lane);
+    }
+    __syncwarp();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
+}
+
+// -------------------------------------------------------- tensor maps ---
+PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
+}
+
+// Tiled map over a K-major uint8 operand [(depth,) rows, K]: box 128 (K) x
+// box_rows, 128-byte swizzle, zero fill outside the tensor.
+bool encode_operand_map(CUtensorMap* map, const void* base, int64_t rows, int64_t K, int64_t depth,
+                        uint32_t box_rows) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = get_encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(depth)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(K) * static_cast<cuuint64_t>(rows)};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(BK), box_rows, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    const cuuint32_t rank = depth > 0 ? 3 : 2;
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, rank, const_cast<void*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+std::once_flag g_attr_once[64];
+
+}  // namespace
+
+int launch_gemm(const GemmArgs& a, int num_sms, int* status_word, cudaStream_t stream, cudaError_t* cuda_err) {
+    *cuda_err = cudaSuccess;
+    int dev = 0;
+    if ((*cuda_err = cudaGetDevice(&dev)) != cudaSuccess) return kErrCuda;
+    if (dev >= 0 && dev < 64) {
+        cudaError_t e = cudaSuccess;
+        std::call_once(g_attr_once[dev], [&] {
+            e = cudaFuncSetAttribute(gemm_blockscaled_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(kSmemBytes));
+            if (e == cudaSuccess)
+                e = cudaFuncSetAttribute(gemm_blockscaled_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kSmemBytes));
+        });
+        if (e != cudaSuccess) {
+            *cuda_err = e;
+            return kErrCuda;
+        }
+    }
+    CUtensorMap tmap_a, tmap_b;
+    std::memset(&tmap_a, 0, sizeof tmap_a);
+    std::memset(&tmap_b, 0, sizeof tmap_b);
+    if (!encode_operand_map(&tmap_a, a.a, a.M, a.K, 0, BM)) return kErrCuda;
+    if (!encode_operand_map(&tmap_b, a.b, a.N, a.K, a.offsets ? a.G : 0, BN)) return kErrCuda;
+    Params p;
+    p.sa = a.sa;
+    p.sb = a.sb;
+    p.sb_stride_n = a.sb_stride_n;
+    p.sb_stride_k = a.sb_stride_k;
+    p.sb_group_stride = a.offsets ? (a.N / 128) * (a.K / 128) : 0;
+    p.bscale = a.bscale;
+    p.d = a.d;
+    p.out_bf16 = a.out_bf16;
+    p.M = a.M;
+    p.N = a.N;
+    p.K = a.K;
+    p.offsets = a.offsets;
+    p.G = a.G;
+    p.m_fastest = a.offsets ? 0 : 1;
+    p.status = status_word;
+    p.limit_ns = kWaitLimitNs;
+    const int64_t tiles = (a.M / BM) * ((a.N + BN - 1) / BN);
+    const int64_t grid = tiles < num_sms ? tiles : num_sms;
+    if (grid <= 0) return kOk;
+    if (a.bscale == 1)
+        gemm_blockscaled_kernel<1><<<static_cast<unsigned>(grid), THREADS, kSmemBytes, stream>>>(tmap_a, tmap_b, p);
+    else
+        gemm_blockscaled_kernel<0><<<static_cast<unsigned>(grid), THREADS, kSmemBytes, stream>>>(tmap_a, tmap_b, p);
+    *cuda_err = cudaPeekAtLastError();
+    return *cuda_err == cudaSuccess ? kOk : kErrCuda;
+}
+
+// ------------------------------------------------- watchdog self-test ---
+namespace {
+__global__ void watchdog_kernel(uint64_t limit_ns, int* status) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bar), 1);
+        abort_flag = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+    // nobody arrives: the phase never completes and the wait must give up
+    if (threadIdx.x == 0) mbar_wait_bounded(smem_u32(&bar), 0, &abort_flag, status, limit_ns, kErrTimeout);
+    __syncthreads();
+}
+}  // namespace
+
+cudaError_t launch_watchdog_selftest(uint64_t timeout_ns, int* status_word, cudaStream_t stream) {
+    watchdog_kernel<<<1, 32, 0, stream>>>(timeout_ns, status_word);
+    return cudaPeekAtLastError();
+}
+
+}  // namespace fp8fg

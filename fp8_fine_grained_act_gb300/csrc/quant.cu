@@ -1,0 +1,303 @@
+// quant.cu -- online fine-grained E4M3 quantizers (HBM-bound).
+//
+// One FP32 scale per group, computed from the current group only:
+// s = fl32(amax / 448), codes = E4M3_RNE_satfinite(fl32(x / s)), both
+// divisions IEEE round-to-nearest.  A zero scale stores 0 and codes that keep
+// only the sign of x.
+//   * 1x128 tiles per token per 128 channels, and 128x128 weight blocks:
+//     DeepSeek-V3 FP8 post (innerforce.co.kr), fine-grained quantization,
+//     Figure 7 (a).
+//   * Scales from the current tensor, no history: "Unified E4M3 format in
+//     DeepSeek-V3" (codingmall.com), Dynamic Scaling and Online Quantization.
+//   * 128x1 token-axis groups with a transposed (K-major) output for the
+//     weight-gradient GEMM, whose reduction runs over tokens: "DeepSeek FP8
+//     Training" (arcalunar.github.io), backward pass, Wgrad step 1.
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace fp8fg {
+namespace {
+
+constexpr int kGroup = 128;
+
+FP8FG_DEV float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+FP8FG_DEV float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// Codes of two values under scale s (s > 0), low value in the low byte.
+FP8FG_DEV uint32_t quant_pair(float a, float b, float s) {
+    return cvt_e4m3x2(__fdiv_rn(a, s), __fdiv_rn(b, s));
+}
+
+// Codes when the scale is 0: the sign of each value, nothing else.
+FP8FG_DEV uint32_t sign_pair(float a, float b) {
+    return ((__float_as_uint(a) >> 31) << 7) | ((__float_as_uint(b) >> 31) << 15);
+}
+
+FP8FG_DEV uint32_t quant_quad(float a, float b, float c, float d, float s) {
+    if (s == 0.0f) return sign_pair(a, b) | (sign_pair(c, d) << 16);
+    return quant_pair(a, b, s) | (quant_pair(c, d, s) << 16);
+}
+
+// ------------------------------------------------------------ 1 x 128 ----
+// A half-warp owns one group (16 lanes x 8 BF16 = 256 bytes); each thread
+// keeps kU groups' loads in flight.  Group index g = c * rows + i, so the
+// scale of group g is scales[g] and consecutive half-warps write consecutive
+// scales.
+constexpr int kRowU = 4;
+
+__global__ void __launch_bounds__(256) quant_act_rows_kernel(const uint4* __restrict__ x, int64_t rows,
+                                                             int64_t cols, uint2* __restrict__ q,
+                                                             float* __restrict__ scales) {
+    const int64_t ng = cols / kGroup;
+    const int64_t total = rows * ng;
+    const int l16 = threadIdx.x & 15;
+    const int64_t hw = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 4;
+    const int64_t nhw = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 4;
+    // both half-warps of a warp run the same iterations (the shuffles below
+    // need the whole warp); the loop is driven by the warp's first half
+    for (int64_t base = hw & ~int64_t(1); base < total; base += nhw * kRowU) {
+        const int64_t g0 = base + (hw & 1);
+        uint4 v[kRowU];
+        int64_t off[kRowU];
+#pragma unroll
+        for (int u = 0; u < kRowU; ++u) {
+            const int64_t g = g0 + u * nhw;
+            off[u] = -1;
+            v[u] = make_uint4(0, 0, 0, 0);
+            if (g < total) {
+                const int64_t c = g / rows, i = g - c * rows;
+                off[u] = (i * cols + c * kGroup) / 8 + l16;  // in units of 8 elements
+                v[u] = __ldcs(x + off[u]);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kRowU; ++u) {
+            const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+            float f[8];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                f[2 * k] = bf16_lo(w[k]);
+                f[2 * k + 1] = bf16_hi(w[k]);
+            }
+            float amax = 0.0f;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) amax = fmaxf(amax, fabsf(f[k]));
+            // every lane of the warp takes part in the shuffles; xor < 16
+            // stays inside the half-warp that owns the group
+#pragma unroll
+            for (int m = 8; m >= 1; m >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, m));
+            if (off[u] < 0) continue;
+            const float s = __fdiv_rn(amax, 448.0f);
+            uint2 out;
+            out.x = quant_quad(f[0], f[1], f[2], f[3], s);
+            out.y = quant_quad(f[4], f[5], f[6], f[7], s);
+            __stcs(q + off[u], out);
+            if (l16 == 0) scales[g0 + u * nhw] = s;
+        }
+    }
+}
+
+// ------------------------------------------------------------ 128 x 1 ----
+// A CTA owns a tile of 128 tokens x 64 channels.  The BF16 tile is staged in
+// shared memory (rows of 32 words + 1 pad word: conflict-free both ways),
+// each thread reduces 16 tokens of a channel pair, the 8 partial maxima meet
+// in shared memory, and each thread writes 16 codes per channel as one
+// 16-byte store into the transposed output q[cols, rows].
+constexpr int kColTileC = 64;
+
+__global__ void __launch_bounds__(256) quant_act_cols_kernel(const uint4* __restrict__ x, int64_t rows,
+                                                             int64_t cols, uint8_t* __restrict__ q,
+                                                             float* __restrict__ scales) {
+    __shared__ uint32_t tile[kGroup][kColTileC / 2 + 1];
+    __shared__ float part[8][kColTileC];
+    const int t = threadIdx.x;
+    const int64_t n_tb = rows / kGroup;
+    const int64_t n_cb = (cols + kColTileC - 1) / kColTileC;
+    for (int64_t tid = blockIdx.x; tid < n_tb * n_cb; tid += gridDim.x) {
+        const int64_t tb = tid % n_tb, cb = tid / n_tb;
+        const int64_t r0 = tb * kGroup, c0 = cb * kColTileC;
+        // load: 8 lanes x 16 bytes per row, 32 rows per pass, 4 passes
+        uint4 v[4];
+        const int vcol = (t & 7) * 8;
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+            const int r = (t >> 3) + 32 * p;
+            v[p] = make_uint4(0, 0, 0, 0);
+            if (c0 + vcol < cols) v[p] = __ldcs(x + ((r0 + r) * cols + c0 + vcol) / 8);
+        }
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+            const int r = (t >> 3) + 32 * p;
+            uint32_t* dst = &tile[r][(t & 7) * 4];
+            dst[0] = v[p].x;
+            dst[1] = v[p].y;
+            dst[2] = v[p].z;
+            dst[3] = v[p].w;
+        }
+        __syncthreads();
+        const int cp = t & 31;  // channel pair: channels 2cp, 2cp+1 of the tile
+        const int rs = t >> 5;  // token segment: tokens 16rs .. 16rs+15
+        float lo[16], hi[16];
+        float a0 = 0.0f, a1 = 0.0f;
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+            const uint32_t w = tile[16 * rs + r][cp];
+            lo[r] = bf16_lo(w);
+            hi[r] = bf16_hi(w);
+            a0 = fmaxf(a0, fabsf(lo[r]));
+            a1 = fmaxf(a1, fabsf(hi[r]));
+        }
+        part[rs][2 * cp] = a0;
+        part[rs][2 * cp + 1] = a1;
+        __syncthreads();
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            a0 = fmaxf(a0, part[k][2 * cp]);
+            a1 = fmaxf(a1, part[k][2 * cp + 1]);
+        }
+        const float s0 = __fdiv_rn(a0, 448.0f), s1 = __fdiv_rn(a1, 448.0f);
+        const int64_t ch0 = c0 + 2 * cp;
+        if (ch0 < cols) {
+            uint4 o;
+            o.x = quant_quad(lo[0], lo[1], lo[2], lo[3], s0);
+            o.y = quant_quad(lo[4], lo[5], lo[6], lo[7], s0);
+            o.z = quant_quad(lo[8], lo[9], lo[10], lo[11], s0);
+            o.w = quant_quad(lo[12], lo[13], lo[14], lo[15], s0);
+            __stcs(reinterpret_cast<uint4*>(q + ch0 * rows + r0 + 16 * rs), o);
+            if (rs == 0) scales[tb * cols + ch0] = s0;
+        }
+        if (ch0 + 1 < cols) {
+            uint4 o;
+            o.x = quant_quad(hi[0], hi[1], hi[2], hi[3], s1);
+            o.y = quant_quad(hi[4], hi[5], hi[6], hi[7], s1);
+            o.z = quant_quad(hi[8], hi[9], hi[10], hi[11], s1);
+            o.w = quant_quad(hi[12], hi[13], hi[14], hi[15], s1);
+            __stcs(reinterpret_cast<uint4*>(q + (ch0 + 1) * rows + r0 + 16 * rs), o);
+            if (rs == 0) scales[tb * cols + ch0 + 1] = s1;
+        }
+        __syncthreads();  // tile and part are reused by the next tile
+    }
+}
+
+// ---------------------------------------------------------- 128 x 128 ----
+// A CTA of 512 threads owns one 128x128 FP32 block at a time and keeps it in
+// registers: thread t holds columns 4(t%32)..+3 of rows 4(t/32)+{0..3} and
+// 64 + 4(t/32)+{0..3}.  Block amax: warp shuffles, then 16 partials in
+// shared memory.  The optional transposed copy goes through a shared tile of
+// 4x4-byte-transposed words.
+__global__ void __launch_bounds__(512) quant_w_kernel(const float4* __restrict__ w, int64_t rows, int64_t cols,
+                                                      uint32_t* __restrict__ q, uint8_t* __restrict__ q_t,
+                                                      float* __restrict__ scales) {
+    __shared__ float red[16];
+    __shared__ uint32_t tq[kGroup][kGroup / 4 + 1];
+    const int t = threadIdx.x, lane = t & 31, wid = t >> 5;
+    const int64_t nbr = rows / kGroup, nbc = cols / kGroup;
+    for (int64_t blk = blockIdx.x; blk < nbr * nbc; blk += gridDim.x) {
+        const int64_t br = blk / nbc, bc = blk - br * nbc;
+        const int64_t r0 = br * kGroup, c0 = bc * kGroup;
+        float4 v[8];
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int64_t r = r0 + 64 * h + 4 * wid + k;
+                v[4 * h + k] = __ldcs(w + (r * cols + c0) / 4 + lane);
+            }
+        float amax = 0.0f;
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+            amax = fmaxf(fmaxf(amax, fmaxf(fabsf(v[k].x), fabsf(v[k].y))), fmaxf(fabsf(v[k].z), fabsf(v[k].w)));
+#pragma unroll
+        for (int m = 16; m >= 1; m >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, m));
+        if (lane == 0) red[wid] = amax;
+        __syncthreads();
+        amax = red[0];
+#pragma unroll
+        for (int k = 1; k < 16; ++k) amax = fmaxf(amax, red[k]);
+        const float s = __fdiv_rn(amax, 448.0f);
+        uint32_t code[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) code[k] = quant_quad(v[k].x, v[k].y, v[k].z, v[k].w, s);
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int64_t r = r0 + 64 * h + 4 * wid + k;
+                __stcs(q + (r * cols + c0) / 4 + lane, code[4 * h + k]);
+            }
+        if (t == 0) scales[br * nbc + bc] = s;
+        if (q_t != nullptr) {
+            // transpose each 4x4 byte block: word k holds row k, byte u = column u
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const uint32_t w0 = code[4 * h], w1 = code[4 * h + 1], w2 = code[4 * h + 2], w3 = code[4 * h + 3];
+                const uint32_t lo01 = __byte_perm(w0, w1, 0x5140), hi01 = __byte_perm(w0, w1, 0x7362);
+                const uint32_t lo23 = __byte_perm(w2, w3, 0x5140), hi23 = __byte_perm(w2, w3, 0x7362);
+                // column u word: bytes (row0,u),(row1,u),(row2,u),(row3,u)
+                const uint32_t c0w = __byte_perm(lo01, lo23, 0x5410);
+                const uint32_t c1w = __byte_perm(lo01, lo23, 0x7632);
+                const uint32_t c2w = __byte_perm(hi01, hi23, 0x5410);
+                const uint32_t c3w = __byte_perm(hi01, hi23, 0x7632);
+                const int rw = 16 * h + wid;  // word index along rows: rows 4*rw .. 4*rw+3
+                tq[4 * lane + 0][rw] = c0w;
+                tq[4 * lane + 1][rw] = c1w;
+                tq[4 * lane + 2][rw] = c2w;
+                tq[4 * lane + 3][rw] = c3w;
+            }
+            __syncthreads();
+            // q_t row (c0 + j) receives the block's column j: 128 bytes = 32 words
+            const int j = t >> 2, part = t & 3;
+            uint4 o0, o1;
+            o0.x = tq[j][8 * part + 0];
+            o0.y = tq[j][8 * part + 1];
+            o0.z = tq[j][8 * part + 2];
+            o0.w = tq[j][8 * part + 3];
+            o1.x = tq[j][8 * part + 4];
+            o1.y = tq[j][8 * part + 5];
+            o1.z = tq[j][8 * part + 6];
+            o1.w = tq[j][8 * part + 7];
+            uint4* dst = reinterpret_cast<uint4*>(q_t + (c0 + j) * rows + r0 + 32 * part);
+            __stcs(dst, o0);
+            __stcs(dst + 1, o1);
+        }
+        __syncthreads();  // red and tq are reused by the next block
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_quant_act_rows(const void* x, int64_t rows, int64_t cols, uint8_t* q, float* scales, int num_sms,
+                                  cudaStream_t stream) {
+    const int64_t groups = rows * (cols / kGroup);
+    const int64_t per_cta = 16 * kRowU;
+    int64_t grid = (groups + per_cta - 1) / per_cta;
+    if (grid > static_cast<int64_t>(num_sms) * 8) grid = static_cast<int64_t>(num_sms) * 8;
+    quant_act_rows_kernel<<<static_cast<unsigned>(grid), 256, 0, stream>>>(
+        static_cast<const uint4*>(x), rows, cols, reinterpret_cast<uint2*>(q), scales);
+    return cudaPeekAtLastError();
+}
+
+cudaError_t launch_quant_act_cols(const void* x, int64_t rows, int64_t cols, uint8_t* q, float* scales, int num_sms,
+                                  cudaStream_t stream) {
+    const int64_t tiles = (rows / kGroup) * ((cols + kColTileC - 1) / kColTileC);
+    int64_t grid = tiles;
+    if (grid > static_cast<int64_t>(num_sms) * 8) grid = static_cast<int64_t>(num_sms) * 8;
+    quant_act_cols_kernel<<<static_cast<unsigned>(grid), 256, 0, stream>>>(static_cast<const uint4*>(x), rows, cols,
+                                                                           q, scales);
+    return cudaPeekAtLastError();
+}
+
+cudaError_t launch_quant_w(const float* w, int64_t rows, int64_t cols, uint8_t* q, uint8_t* q_t, float* scales,
+                           int num_sms, cudaStream_t stream) {
+    const int64_t blocks = (rows / kGroup) * (cols / kGroup);
+    int64_t grid = blocks;
+    if (grid > static_cast<int64_t>(num_sms) * 4) grid = static_cast<int64_t>(num_sms) * 4;
+    quant_w_kernel<<<static_cast<unsigned>(grid), 512, 0, stream>>>(reinterpret_cast<const float4*>(w), rows, cols,
+                                                                    reinterpret_cast<uint32_t*>(q), q_t, scales);
+    return cudaPeekAtLastError();
+}
+
+}  // namespace fp8fg

@@ -1,0 +1,186 @@
+/*
+ * fp8fg.h -- C ABI of the GB300 (sm_103a) fine-grained FP8 quantization and
+ * block-scaled FP8 GEMM library (libfp8fg.so).
+ *
+ * The method: online E4M3 quantization with one FP32 scale per group,
+ * s = amax / 448 of the current group (no history), 1x128 tiles for
+ * activations and gradients and 128x128 blocks for FP32 master weights; then
+ * an FP8 GEMM that accumulates each 128-wide K chunk on the tensor cores,
+ * multiplies the chunk's partial sums by the two group scales and promotes
+ * them into FP32 accumulators, writing FP32 or BF16.
+ *   - DeepSeek-V3 FP8 post (innerforce.co.kr), fine-grained quantization,
+ *     Figure 7 (a): 1x128 tiles per token per 128 channels, 128x128 blocks
+ *     per 128 input x 128 output channels, max-abs scaled to the FP8 maximum;
+ *     the increased-precision accumulation paragraph (FP8 MMA on H800 keeps
+ *     about 14 bits, so partial sums are promoted to FP32).
+ *   - "DeepSeek FP8 Training" (arcalunar.github.io): the Fprop, Wgrad and
+ *     Dgrad pipelines (operand roles, FP32 accumulation, BF16 / FP32 outputs).
+ *   - "Unified E4M3 format in DeepSeek-V3" (codingmall.com): E4M3 for every
+ *     tensor, online scales, promotion of partial results to FP32 registers
+ *     at fixed intervals (Fine-Grained Quantization Strategy; Dynamic Scaling
+ *     and Online Quantization; Enhanced Numerical Stability).
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are DEVICE pointers (CUDA global memory), owned by
+ *     the caller, who allocates every buffer.  Entry points allocate nothing
+ *     and keep no per-call state.  Row-major layouts, last index contiguous.
+ *   - All calls are asynchronous on `stream` (0 = the legacy default stream)
+ *     and stream-ordered; none synchronises the host.  They are thread-safe.
+ *   - Shapes are element counts (int64).  Returned: an fp8fg_status.  Argument
+ *     errors are detected on the host before anything is launched, and then
+ *     nothing is written.  A device that is not compute capability 10.3 gives
+ *     FP8FG_ERR_UNSUPPORTED_DEVICE (there is no fallback path).
+ *   - Every bounded wait inside a kernel that runs out of time records
+ *     FP8FG_ERR_TIMEOUT in a library-owned device status word, which
+ *     fp8fg_last_device_status() reads; such a kernel returns without hanging.
+ *   - E4M3 is the OCP FP8 E4M3 format (bias 7, max 448, no infinities).
+ *     Element codes are enc_RNE_satfinite(fl32(x / s)) with an IEEE division;
+ *     a group whose scale is 0 (all zeros, or amax/448 underflowing in FP32)
+ *     stores s = 0 and codes that keep only the sign of x.  Inputs are finite
+ *     (NaN/Inf input gives unspecified codes).
+ */
+#ifndef FP8FG_H
+#define FP8FG_H
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FP8FG_OK = 0,
+    FP8FG_ERR_INVALID_ARG = 1,        /* null pointer, bad enum, negative or non-tiling shape */
+    FP8FG_ERR_MISALIGNED = 2,         /* a pointer is not 16-byte aligned */
+    FP8FG_ERR_UNSUPPORTED_DEVICE = 3, /* current device is not sm_103 */
+    FP8FG_ERR_CUDA = 4,               /* a CUDA runtime/driver call or a launch failed */
+    FP8FG_ERR_TIMEOUT = 5             /* (device status) a bounded wait ran out */
+} fp8fg_status;
+
+typedef enum { FP8FG_OUT_F32 = 0, FP8FG_OUT_BF16 = 1 } fp8fg_out_dtype;
+
+/* Grouping axis of the activation quantizer. */
+typedef enum {
+    FP8FG_AXIS_COLS = 0, /* 1x128: groups of 128 consecutive columns of one row */
+    FP8FG_AXIS_ROWS = 1  /* 128x1: groups of 128 consecutive rows of one column; output transposed */
+} fp8fg_axis;
+
+/* How the GEMM's B operand is scaled. */
+typedef enum {
+    FP8FG_BSCALE_BLOCK128 = 0, /* one scale per 128 (N) x 128 (K) block */
+    FP8FG_BSCALE_ROW = 1       /* one scale per row of B per 128-wide K chunk */
+} fp8fg_bscale;
+
+/*
+ * fp8_quant_act_1x128 -- online E4M3 quantization of a BF16 activation or
+ * gradient x[rows, cols] (row-major, 2-byte elements).
+ *   axis FP8FG_AXIS_COLS (Fprop X, Dgrad dY; "per token per 128 channels",
+ *   Figure 7 (a) of the DeepSeek-V3 FP8 post):
+ *     requires cols % 128 == 0 (rows >= 0 arbitrary);
+ *     q[rows, cols] uint8 E4M3 codes;
+ *     scales[cols/128, rows] float32: scales[c*rows + i] belongs to the group
+ *     x[i, 128c .. 128c+127].
+ *   axis FP8FG_AXIS_ROWS (Wgrad operands, whose reduction runs over tokens:
+ *   "DeepSeek FP8 Training", backward pass step 1):
+ *     requires rows % 128 == 0 and cols % 8 == 0 (16-byte rows of x);
+ *     q[cols, rows] uint8, i.e. the codes TRANSPOSED (K-major for the Wgrad GEMM);
+ *     scales[rows/128, cols] float32: scales[t*cols + j] belongs to the group
+ *     x[128t .. 128t+127, j].
+ * x, q and scales must be 16-byte aligned.  rows == 0 or cols == 0 is a no-op.
+ */
+int fp8_quant_act_1x128(const void *x_bf16, int64_t rows, int64_t cols, int axis,
+                        uint8_t *q, float *scales, cudaStream_t stream);
+
+/*
+ * fp8_quant_w_128x128 -- online E4M3 quantization of an FP32 master weight
+ * w[rows, cols] in 128x128 blocks ("per 128 input channels per 128 output
+ * channels", Figure 7 (a) of the DeepSeek-V3 FP8 post; the FP32 master is
+ * cast to FP8 each step: "DeepSeek FP8 Training", forward step 2).
+ *   requires rows % 128 == 0 and cols % 128 == 0;
+ *   q[rows, cols] uint8 E4M3 codes;
+ *   q_t: NULL, or q_t[cols, rows] uint8 receiving the same codes transposed
+ *        (the K-major B operand of the Dgrad GEMM; a block's scale is the
+ *        same in both orientations);
+ *   scales[rows/128, cols/128] float32, row-major.
+ * All pointers 16-byte aligned.  rows == 0 or cols == 0 is a no-op.
+ */
+int fp8_quant_w_128x128(const float *w, int64_t rows, int64_t cols,
+                        uint8_t *q, uint8_t *q_t, float *scales, cudaStream_t stream);
+
+/*
+ * fp8_gemm_blockscaled -- D[M, N] = A[M, K] . B[N, K]^T with per-group
+ * scales, both operands K-major E4M3 ("DeepSeek FP8 Training": Fprop
+ * Y = X W^T, Dgrad dX = dY W, Wgrad dW = dY^T X).  For every 128-wide K
+ * chunk c the tensor cores form P = sum_{k in c} a[i,k] b[j,k] in FP32 and
+ * the kernel adds P * (sa[c, i] * sb(j, c)) into FP32 accumulators (the
+ * promotion at fixed intervals of "Unified E4M3 format in DeepSeek-V3",
+ * Enhanced Numerical Stability; interval = one 128-wide group).
+ *   a[M, K] uint8, sa[K/128, M] float32 (the layout fp8_quant_act_1x128 writes);
+ *   b[N, K] uint8;
+ *   bscale FP8FG_BSCALE_BLOCK128: sb(j, c) = sb[(j/128)*sb_stride_n + c*sb_stride_k]
+ *     (a weight's [N/128, K/128] scales: strides (K/128, 1); Dgrad reads the
+ *     same array transposed with strides (1, N_w/128));
+ *   bscale FP8FG_BSCALE_ROW: sb(j, c) = sb[c*N + j], sb[K/128, N] (the
+ *     layout of the 128x1 activation quantizer; Wgrad);
+ *     sb_stride_n and sb_stride_k are ignored;
+ *   d[M, N]: float32 (out_dtype FP8FG_OUT_F32) or bfloat16 rounded to
+ *     nearest even (FP8FG_OUT_BF16).
+ * Requires M % 128 == 0, N % 128 == 0, K % 128 == 0 (tokens are padded to
+ * 128 by the caller); all pointers 16-byte aligned; sb strides >= 0.
+ * K == 0 writes zeros.  M == 0 or N == 0 is a no-op.
+ * Accuracy (tested): |d - o| <= 2^-16 * sum_k |a~ b~| for FP32 output, plus
+ * one BF16 spacing of o for BF16 output, o being the exact sum of the
+ * dequantized products.
+ */
+int fp8_gemm_blockscaled(const uint8_t *a, const float *sa,
+                         const uint8_t *b, const float *sb, int bscale,
+                         int64_t sb_stride_n, int64_t sb_stride_k,
+                         void *d, int out_dtype, int64_t M, int64_t N, int64_t K,
+                         cudaStream_t stream);
+
+/*
+ * fp8_gemm_grouped -- grouped MoE-expert GEMM: rows [off[g], off[g+1]) of A
+ * multiply expert weight g: D[r, :] = A[r, :] . B[g]^T with 128x128 block
+ * scales (MoE training with FP8 activations, DeepSeek-V3 FP8 post; one
+ * weight per expert, tokens grouped contiguously per expert).
+ *   a[M_total, K] uint8, sa[K/128, M_total];
+ *   b[G, N, K] uint8, sb[G, N/128, K/128] float32;
+ *   group_offsets: DEVICE int32[G+1], non-decreasing, off[0] = 0,
+ *     off[G] = M_total, every entry a multiple of 128 (groups padded with
+ *     zero rows); empty groups allowed;
+ *   d[M_total, N] float32 or bfloat16.
+ * Requires M_total % 128 == 0, N % 128 == 0, K % 128 == 0, 1 <= G <= 4096.
+ * Offsets that break these rules are detected on the device: the kernel
+ * records FP8FG_ERR_INVALID_ARG in the device status word and writes nothing.
+ */
+int fp8_gemm_grouped(const uint8_t *a, const float *sa,
+                     const uint8_t *b, const float *sb,
+                     const int32_t *group_offsets, int G,
+                     void *d, int out_dtype, int64_t M_total, int64_t N, int64_t K,
+                     cudaStream_t stream);
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char *fp8fg_status_string(int status);
+
+/*
+ * fp8fg_last_device_status -- read and clear the device status word of the
+ * current device (an asynchronous error recorded by a kernel: a bounded
+ * wait that ran out, or invalid grouped offsets).  Synchronises `stream`.
+ * Returns FP8FG_OK when no kernel recorded anything since the last read.
+ */
+int fp8fg_last_device_status(cudaStream_t stream);
+
+/*
+ * fp8fg_selftest_watchdog -- test hook for the kernels' bounded waits: runs a
+ * one-warp kernel that waits on an mbarrier nobody arrives on, with a limit
+ * of `timeout_ns` nanoseconds (1 .. 10^9).  The wait gives up, records
+ * FP8FG_ERR_TIMEOUT in the device status word and the kernel returns.
+ * The caller reads it with fp8fg_last_device_status().  No fault, no trap.
+ */
+int fp8fg_selftest_watchdog(int64_t timeout_ns, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FP8FG_H */

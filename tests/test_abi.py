@@ -1,0 +1,116 @@
+"""The C ABI without a GPU: the library builds and loads, exports every entry
+point include/fp8fg.h declares, and rejects bad arguments on the host before
+touching a device.  No compute call is made here."""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fp8fg.h")
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b([a-z_][a-z0-9_]*)\s*\(", text, flags=re.M)
+    return sorted(set(n for n in names if n.startswith("fp8")))
+
+
+def test_header_declares_the_entry_points():
+    names = _declared_functions()
+    for n in ["fp8_quant_act_1x128", "fp8_quant_w_128x128", "fp8_gemm_blockscaled", "fp8_gemm_grouped",
+              "fp8fg_status_string", "fp8fg_last_device_status", "fp8fg_selftest_watchdog"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(cuda_lib_path):
+    lib = ctypes.CDLL(cuda_lib_path)
+    for n in _declared_functions():
+        assert hasattr(lib, n), f"{n} declared in fp8fg.h but not exported"
+    from fp8_fine_grained_act_gb300 import binding
+    assert set(binding.SIGNATURES) == set(_declared_functions())
+
+
+def test_status_strings(cuda_lib_path):
+    from fp8_fine_grained_act_gb300 import binding as b
+    for code, word in [(0, "OK"), (1, "INVALID_ARG"), (2, "MISALIGNED"), (3, "UNSUPPORTED"), (4, "CUDA"),
+                       (5, "TIMEOUT")]:
+        assert word in b.status_string(code)
+    assert "unknown" in b.status_string(99)
+
+
+@pytest.fixture(scope="module")
+def lib(cuda_lib_path):
+    from fp8_fine_grained_act_gb300 import binding as b
+    return b.load()
+
+
+A16 = 0x10000          # a 16-byte aligned fake address: never dereferenced (rejected before any launch)
+MIS = 0x10008          # an 8-byte aligned fake address
+
+
+def test_quant_act_argument_checks(lib):
+    f = lib.fp8_quant_act_1x128
+    assert f(A16, 4, 100, 0, A16, A16, None) == 1          # cols not a multiple of 128
+    assert f(A16, 100, 8, 1, A16, A16, None) == 1          # rows not a multiple of 128 for 128x1
+    assert f(A16, 128, 12, 1, A16, A16, None) == 1         # cols not a multiple of 8 for 128x1
+    assert f(A16, 4, 128, 2, A16, A16, None) == 1          # bad axis
+    assert f(A16, -1, 128, 0, A16, A16, None) == 1
+    assert f(None, 4, 128, 0, A16, A16, None) == 1         # null input
+    assert f(A16, 4, 128, 0, None, A16, None) == 1
+    assert f(A16, 4, 128, 0, A16, None, None) == 1
+    assert f(MIS, 4, 128, 0, A16, A16, None) == 2          # misaligned
+    assert f(A16, 4, 128, 0, MIS, A16, None) == 2
+    assert f(None, 0, 128, 0, None, None, None) == 0       # empty: no-op, nothing touched
+    assert f(None, 4, 0, 0, None, None, None) == 0
+
+
+def test_quant_w_argument_checks(lib):
+    f = lib.fp8_quant_w_128x128
+    assert f(A16, 128, 100, A16, None, A16, None) == 1
+    assert f(A16, 100, 128, A16, None, A16, None) == 1
+    assert f(None, 128, 128, A16, None, A16, None) == 1
+    assert f(A16, 128, 128, A16, MIS, A16, None) == 2      # misaligned transposed output
+    assert f(A16, 0, 128, None, None, None, None) == 0
+
+
+def test_gemm_argument_checks(lib):
+    f = lib.fp8_gemm_blockscaled
+    ok = dict(a=A16, sa=A16, b=A16, sb=A16, bscale=0, sn=1, sk=1, d=A16, od=1, M=128, N=128, K=128)
+
+    def call(**kw):
+        v = dict(ok, **kw)
+        return f(v["a"], v["sa"], v["b"], v["sb"], v["bscale"], v["sn"], v["sk"], v["d"], v["od"],
+                 v["M"], v["N"], v["K"], None)
+
+    assert call(M=100) == 1 and call(N=200) == 1 and call(K=130) == 1
+    assert call(M=-128) == 1
+    assert call(od=7) == 1 and call(bscale=3) == 1
+    assert call(sn=-1) == 1
+    assert call(a=None) == 1 and call(sb=None) == 1 and call(d=None) == 1
+    assert call(a=MIS) == 2 and call(d=MIS) == 2 and call(sa=MIS) == 2
+    assert call(M=0, a=None, d=None) == 0                  # empty: no-op
+    assert call(M=1 << 32) == 1                            # beyond the supported range
+    g = lib.fp8_gemm_grouped
+    assert g(A16, A16, A16, A16, A16, 0, A16, 1, 128, 128, 128, None) == 1       # G < 1
+    assert g(A16, A16, A16, A16, None, 4, A16, 1, 128, 128, 128, None) == 1      # no offsets
+    assert g(A16, A16, A16, A16, A16 + 2, 4, A16, 1, 128, 128, 128, None) == 2   # offsets not 4-aligned
+    assert g(A16, A16, A16, A16, A16, 4, A16, 1, 100, 128, 128, None) == 1
+
+
+def test_watchdog_argument_checks(lib):
+    assert lib.fp8fg_selftest_watchdog(0, None) == 1
+    assert lib.fp8fg_selftest_watchdog(2_000_000_000, None) == 1
+
+
+def test_no_device_means_an_error_not_a_fallback(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    # valid arguments reach the device probe, which fails: no CPU path exists
+    st = lib.fp8_quant_act_1x128(A16, 4, 128, 0, A16, A16, None)
+    assert st in (3, 4)
