@@ -72,6 +72,8 @@ int fp8_quant_act_1x128(const void* x_bf16, int64_t rows, int64_t cols, int axis
     if (rows == 0 || cols == 0) return kOk;
     if (!x_bf16 || !q || !scales) return kErrInvalidArg;
     if (rows > (int64_t(1) << 40) / cols) return kErrInvalidArg;
+    // the 1x128 kernel's grid: (rows / 64) blocks by (cols / 128) group columns
+    if (axis == FP8FG_AXIS_COLS && (cols / 128 > 65535 || rows / 64 >= (int64_t(1) << 31))) return kErrInvalidArg;
     if (!aligned16(x_bf16) || !aligned16(q) || !aligned16(scales)) return kErrMisaligned;
     DeviceInfo* d = nullptr;
     int st = current_device(&d);

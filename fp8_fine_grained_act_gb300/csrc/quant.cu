@@ -26,77 +26,97 @@ constexpr int kGroup = 128;
 FP8FG_DEV float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 FP8FG_DEV float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
-// Codes of two values under scale s (s > 0), low value in the low byte.
-FP8FG_DEV uint32_t quant_pair(float a, float b, float s) {
-    return cvt_e4m3x2(__fdiv_rn(a, s), __fdiv_rn(b, s));
-}
+// Division by the group scale.  The element code needs fl32(x / s) exactly
+// (an IEEE round-to-nearest quotient).  For a normal scale it is computed
+// with the reciprocal correction of Markstein ("Computation of elementary
+// functions on the IBM RISC System/6000 processor", IBM J. Res. Dev. 1990):
+// with r = RN(1/s) (correctly rounded reciprocal, computed once per group)
+// and q = RN(x r), which is within one ulp of x / s, the remainder
+// x - s q is exact in one FMA and RN(q + (x - s q) r) is the correctly
+// rounded quotient.  The remainder stays exact (no underflow) whenever
+// |x / s| >= 2^-11 and s >= 2^-90; smaller quotients all encode to a signed
+// zero in E4M3 (its smallest magnitude is 2^-9, the tie to zero at 2^-10),
+// and the sign of the quotient is the sign of x (s > 0), so the result is
+// taken with x's sign.  Scales below 2^-90 fall back to the full IEEE
+// division.  Bit-exactness against the oracle's IEEE division is tested.
+struct GroupScale {
+    float s, r;
+    int mode;  // 0: s == 0 (codes keep only the sign), 1: reciprocal correction, 2: IEEE division
+    FP8FG_DEV explicit GroupScale(float scale) : s(scale), r(0.0f) {
+        if (s == 0.0f) {
+            mode = 0;
+        } else if (s >= 0x1p-90f) {
+            mode = 1;
+            r = __frcp_rn(s);
+        } else {
+            mode = 2;
+        }
+    }
+    FP8FG_DEV float quot(float x) const {
+        if (mode == 2) return __fdiv_rn(x, s);
+        const float q = x * r;
+        const float rem = fmaf(-q, s, x);
+        return copysignf(fmaf(rem, r, q), x);
+    }
+};
 
 // Codes when the scale is 0: the sign of each value, nothing else.
 FP8FG_DEV uint32_t sign_pair(float a, float b) {
     return ((__float_as_uint(a) >> 31) << 7) | ((__float_as_uint(b) >> 31) << 15);
 }
 
-FP8FG_DEV uint32_t quant_quad(float a, float b, float c, float d, float s) {
-    if (s == 0.0f) return sign_pair(a, b) | (sign_pair(c, d) << 16);
-    return quant_pair(a, b, s) | (quant_pair(c, d, s) << 16);
+// Four values -> four E4M3 codes (a in the lowest byte).
+FP8FG_DEV uint32_t quant_quad(float a, float b, float c, float d, const GroupScale& g) {
+    if (g.mode == 0) return sign_pair(a, b) | (sign_pair(c, d) << 16);
+    return static_cast<uint32_t>(cvt_e4m3x2(g.quot(a), g.quot(b))) |
+           (static_cast<uint32_t>(cvt_e4m3x2(g.quot(c), g.quot(d))) << 16);
 }
 
 // ------------------------------------------------------------ 1 x 128 ----
-// A half-warp owns one group (16 lanes x 8 BF16 = 256 bytes); each thread
-// keeps kU groups' loads in flight.  Group index g = c * rows + i, so the
-// scale of group g is scales[g] and consecutive half-warps write consecutive
-// scales.
+// Grid (row blocks of 64, 128-column groups): a CTA owns 64 rows of one
+// group column c.  A half-warp owns one group (16 lanes x 8 BF16 = 256
+// bytes) and keeps kRowU groups' loads in flight; the CTA's 64 scales are
+// contiguous in scales[c * rows + r].
 constexpr int kRowU = 4;
+constexpr int kRowsPerCta = 16 * kRowU;
 
 __global__ void __launch_bounds__(256) quant_act_rows_kernel(const uint4* __restrict__ x, int64_t rows,
                                                              int64_t cols, uint2* __restrict__ q,
                                                              float* __restrict__ scales) {
-    const int64_t ng = cols / kGroup;
-    const int64_t total = rows * ng;
-    const int l16 = threadIdx.x & 15;
-    const int64_t hw = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 4;
-    const int64_t nhw = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 4;
-    // both half-warps of a warp run the same iterations (the shuffles below
-    // need the whole warp); the loop is driven by the warp's first half
-    for (int64_t base = hw & ~int64_t(1); base < total; base += nhw * kRowU) {
-        const int64_t g0 = base + (hw & 1);
-        uint4 v[kRowU];
-        int64_t off[kRowU];
+    const int64_t c = blockIdx.y;
+    const int l16 = threadIdx.x & 15, hw = threadIdx.x >> 4;
+    const int64_t r0 = static_cast<int64_t>(blockIdx.x) * kRowsPerCta + hw;
+    uint4 v[kRowU];
 #pragma unroll
-        for (int u = 0; u < kRowU; ++u) {
-            const int64_t g = g0 + u * nhw;
-            off[u] = -1;
-            v[u] = make_uint4(0, 0, 0, 0);
-            if (g < total) {
-                const int64_t c = g / rows, i = g - c * rows;
-                off[u] = (i * cols + c * kGroup) / 8 + l16;  // in units of 8 elements
-                v[u] = __ldcs(x + off[u]);
-            }
+    for (int u = 0; u < kRowU; ++u) {
+        const int64_t r = r0 + 16 * u;
+        v[u] = make_uint4(0, 0, 0, 0);
+        if (r < rows) v[u] = __ldcs(x + (r * cols + c * kGroup) / 8 + l16);
+    }
+#pragma unroll
+    for (int u = 0; u < kRowU; ++u) {
+        const int64_t r = r0 + 16 * u;
+        const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+        float f[8];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            f[2 * k] = bf16_lo(w[k]);
+            f[2 * k + 1] = bf16_hi(w[k]);
         }
+        float amax = 0.0f;
 #pragma unroll
-        for (int u = 0; u < kRowU; ++u) {
-            const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-            float f[8];
+        for (int k = 0; k < 8; ++k) amax = fmaxf(amax, fabsf(f[k]));
+        // xor < 16 stays inside the half-warp that owns the group
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                f[2 * k] = bf16_lo(w[k]);
-                f[2 * k + 1] = bf16_hi(w[k]);
-            }
-            float amax = 0.0f;
-#pragma unroll
-            for (int k = 0; k < 8; ++k) amax = fmaxf(amax, fabsf(f[k]));
-            // every lane of the warp takes part in the shuffles; xor < 16
-            // stays inside the half-warp that owns the group
-#pragma unroll
-            for (int m = 8; m >= 1; m >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, m));
-            if (off[u] < 0) continue;
-            const float s = __fdiv_rn(amax, 448.0f);
-            uint2 out;
-            out.x = quant_quad(f[0], f[1], f[2], f[3], s);
-            out.y = quant_quad(f[4], f[5], f[6], f[7], s);
-            __stcs(q + off[u], out);
-            if (l16 == 0) scales[g0 + u * nhw] = s;
-        }
+        for (int m = 8; m >= 1; m >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, m));
+        if (r >= rows) continue;
+        const float s = __fdiv_rn(amax, 448.0f);
+        const GroupScale gs(s);
+        uint2 out;
+        out.x = quant_quad(f[0], f[1], f[2], f[3], gs);
+        out.y = quant_quad(f[4], f[5], f[6], f[7], gs);
+        __stcs(q + (r * cols + c * kGroup) / 8 + l16, out);
+        if (l16 == 0) scales[c * rows + r] = s;
     }
 }
 
@@ -159,22 +179,23 @@ __global__ void __launch_bounds__(256) quant_act_cols_kernel(const uint4* __rest
             a1 = fmaxf(a1, part[k][2 * cp + 1]);
         }
         const float s0 = __fdiv_rn(a0, 448.0f), s1 = __fdiv_rn(a1, 448.0f);
+        const GroupScale g0(s0), g1(s1);
         const int64_t ch0 = c0 + 2 * cp;
         if (ch0 < cols) {
             uint4 o;
-            o.x = quant_quad(lo[0], lo[1], lo[2], lo[3], s0);
-            o.y = quant_quad(lo[4], lo[5], lo[6], lo[7], s0);
-            o.z = quant_quad(lo[8], lo[9], lo[10], lo[11], s0);
-            o.w = quant_quad(lo[12], lo[13], lo[14], lo[15], s0);
+            o.x = quant_quad(lo[0], lo[1], lo[2], lo[3], g0);
+            o.y = quant_quad(lo[4], lo[5], lo[6], lo[7], g0);
+            o.z = quant_quad(lo[8], lo[9], lo[10], lo[11], g0);
+            o.w = quant_quad(lo[12], lo[13], lo[14], lo[15], g0);
             __stcs(reinterpret_cast<uint4*>(q + ch0 * rows + r0 + 16 * rs), o);
             if (rs == 0) scales[tb * cols + ch0] = s0;
         }
         if (ch0 + 1 < cols) {
             uint4 o;
-            o.x = quant_quad(hi[0], hi[1], hi[2], hi[3], s1);
-            o.y = quant_quad(hi[4], hi[5], hi[6], hi[7], s1);
-            o.z = quant_quad(hi[8], hi[9], hi[10], hi[11], s1);
-            o.w = quant_quad(hi[12], hi[13], hi[14], hi[15], s1);
+            o.x = quant_quad(hi[0], hi[1], hi[2], hi[3], g1);
+            o.y = quant_quad(hi[4], hi[5], hi[6], hi[7], g1);
+            o.z = quant_quad(hi[8], hi[9], hi[10], hi[11], g1);
+            o.w = quant_quad(hi[12], hi[13], hi[14], hi[15], g1);
             __stcs(reinterpret_cast<uint4*>(q + (ch0 + 1) * rows + r0 + 16 * rs), o);
             if (rs == 0) scales[tb * cols + ch0 + 1] = s1;
         }
@@ -218,9 +239,10 @@ __global__ void __launch_bounds__(512) quant_w_kernel(const float4* __restrict__
 #pragma unroll
         for (int k = 1; k < 16; ++k) amax = fmaxf(amax, red[k]);
         const float s = __fdiv_rn(amax, 448.0f);
+        const GroupScale gs(s);
         uint32_t code[8];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) code[k] = quant_quad(v[k].x, v[k].y, v[k].z, v[k].w, s);
+        for (int k = 0; k < 8; ++k) code[k] = quant_quad(v[k].x, v[k].y, v[k].z, v[k].w, gs);
 #pragma unroll
         for (int h = 0; h < 2; ++h)
 #pragma unroll
@@ -271,12 +293,10 @@ __global__ void __launch_bounds__(512) quant_w_kernel(const float4* __restrict__
 
 cudaError_t launch_quant_act_rows(const void* x, int64_t rows, int64_t cols, uint8_t* q, float* scales, int num_sms,
                                   cudaStream_t stream) {
-    const int64_t groups = rows * (cols / kGroup);
-    const int64_t per_cta = 16 * kRowU;
-    int64_t grid = (groups + per_cta - 1) / per_cta;
-    if (grid > static_cast<int64_t>(num_sms) * 8) grid = static_cast<int64_t>(num_sms) * 8;
-    quant_act_rows_kernel<<<static_cast<unsigned>(grid), 256, 0, stream>>>(
-        static_cast<const uint4*>(x), rows, cols, reinterpret_cast<uint2*>(q), scales);
+    (void)num_sms;
+    const dim3 grid(static_cast<unsigned>((rows + kRowsPerCta - 1) / kRowsPerCta), static_cast<unsigned>(cols / kGroup));
+    quant_act_rows_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint4*>(x), rows, cols,
+                                                    reinterpret_cast<uint2*>(q), scales);
     return cudaPeekAtLastError();
 }
 

@@ -152,3 +152,34 @@ def test_dense_sweep_value_and_group_max(gpu_device):
     n = (len(x) // 4) * 4
     x = x[:n].reshape(-1, 512)
     _act_parity(synth.f32_to_bf16_bits(x), 0, gpu_device)
+
+
+def test_weight_quotients_at_rounding_midpoints(gpu_device):
+    """FP32 weights placed on, and a few ulps around, every E4M3 rounding
+    midpoint times the block scale, for scales with arbitrary mantissas and
+    for scales below 2^-90 (the kernel's full-division path).  Any one-ulp
+    error in the quotient x / s would flip a code here."""
+    grid = oracle.e4m3_decode(np.arange(0x7F, dtype=np.uint8))
+    mids = (grid[1:] + grid[:-1]) / 2                       # rounding midpoints in [2^-10, 464)
+    rng = np.random.default_rng(77)
+    blocks = []
+    amaxes = [np.float32(rng.uniform(1, 2) * 2.0 ** e) for e in (-30, -3, 0, 5, 40)]
+    amaxes += [np.float32(1.3e-28), np.float32(3.0e-29)]     # scale below 2^-90
+    for amax in amaxes:
+        s = np.float32(amax / np.float32(448))              # the block scale the kernel derives
+        vals = []
+        for m in mids:
+            x = np.float32(m * np.float64(s))
+            for k in range(-3, 4):
+                y = x
+                step = np.float32(np.inf) if k > 0 else np.float32(-np.inf)
+                for _ in range(abs(k)):
+                    y = np.nextafter(y, step)
+                if abs(y) <= amax:
+                    vals += [y, -y]
+        vals = np.array(vals, np.float32)
+        blk = np.resize(vals, 128 * 128).reshape(128, 128)
+        blk[0, 0] = amax
+        blocks.append(blk)
+    w = np.concatenate(blocks, axis=1)                      # [128, 128 * n_blocks]
+    _w_parity(np.ascontiguousarray(w), gpu_device)
