@@ -4,7 +4,7 @@
 // scale per 128-wide K chunk (per row of A; per 128x128 block or per row of
 // B).  For every K chunk c the tensor cores accumulate
 //     P = sum_{k in chunk c} a[i, k] b[j, k]        (FP32, in TMEM)
-// and the epilogue warps promote it into FP32 registers:
+// and the promotion warps fold it into FP32 registers:
 //     acc[i, j] += P[i, j] * (sa[c, i] * sb(j, c)).
 // Sources: "DeepSeek FP8 Training" (arcalunar.github.io), forward pipeline
 // steps 3-4 (tile-based FP8 GEMM, FP32 accumulation, BF16 output) and the
@@ -16,20 +16,25 @@
 // at fixed intervals; the interval here is one 128-wide group).
 //
 // Kernel structure (one persistent CTA per SM, 12 warps in 3 warpgroups;
-// warpgroup 0 gives registers to the epilogue warpgroups with setmaxnreg):
+// warpgroup 0 gives registers to the promotion warpgroups with setmaxnreg):
 //   warp 0      TMA producer: A tile [128 x 128 B] and B tile [256 x 128 B]
-//               per K chunk into a 4-stage shared-memory ring (128-byte
-//               swizzle), plus the chunk's A scales (and per-row B scales)
-//               into an 8-slot scale ring, all completing on mbarriers;
+//               per K chunk into a 3-stage shared-memory ring (128-byte
+//               swizzle), plus,
+//               for per-row B scales, the chunk's 256 B scales into a ring
+//               of their own; everything completes on mbarriers;
 //   warp 1      MMA issuer: 4 x tcgen05.mma.kind::f8f6f4 (K = 32 each) per
 //               chunk into one of two 256-column TMEM buffers, then commits
-//               to the stage's "empty" barrier and the buffer's "full" one;
+//               to the stage's "empty" mbarrier and the buffer's "full" one;
 //   warps 2-3   idle;
-//   warps 4-11  epilogue: tcgen05.ld the chunk's partial sums, release the
-//               TMEM buffer, scale-and-add into 128 FP32 registers per
-//               thread (one row, 128 columns), and after the last chunk
-//               convert and store.
-// The MMA of chunk c+1 runs while the epilogue promotes chunk c.
+//   warps 4-11  promotion: wait for the buffer, tcgen05.ld 4 x 32 columns
+//               (the next load in flight while the previous 32 columns are
+//               scaled and added with packed FP32 FMAs), hand the buffer
+//               back (mbarrier), and after the tile's last chunk write the 128 x 256
+//               outputs through shared memory with TMA stores.  The A scales
+//               come straight from global memory, three chunks ahead, into
+//               registers; block B scales come 32 chunks per load, one per
+//               lane, and are broadcast by shuffles.
+// The MMA of chunk c+1 runs while the promotion warps fold chunk c.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
@@ -48,36 +53,43 @@ constexpr int BM = 128;   // rows of A per tile (TMEM lanes)
 constexpr int BN = 256;   // rows of B per tile (TMEM columns per buffer)
 constexpr int BK = 128;   // one quantization group along K
 constexpr int MMA_K = 32; // K per tcgen05.mma for 8-bit operands
-constexpr int STAGES = 4;
-constexpr int SLOTS = 8;
 constexpr int EPI_WARPS = 8;
 constexpr int THREADS = 128 + 32 * EPI_WARPS;
 // registers per thread: 168 at launch (384 x 168 = 64512); after the split
-// warpgroup 0 keeps 64 and the two epilogue warpgroups take 216 each
+// warpgroup 0 keeps 64 and the two promotion warpgroups take 216 each
 // (128 x 64 + 256 x 216 = 63488, within the launch total).
 constexpr int REGS_LOW = 64, REGS_HIGH = 216;
 constexpr uint32_t TMEM_COLS = 2 * BN;
 constexpr uint32_t A_BYTES = BM * BK;
 constexpr uint32_t B_BYTES = BN * BK;
 
+// Shared memory.  kRowB = 1 (B scales per row of B) also keeps a ring of
+// the chunks' B scales.  (Three operand stages measured faster than four on
+// the Fprop shape: the fourth leaves almost no L1 for the scale loads.)
+template <int kRowB>
 struct __align__(1024) Smem {
-    uint8_t a[STAGES][A_BYTES];
-    uint8_t b[STAGES][B_BYTES];
-    float sa[SLOTS][BM];
-    float sb[SLOTS][BN];
-    uint64_t full[STAGES];
-    uint64_t empty[STAGES];
+    static constexpr int kStages = 3;
+    static constexpr int kSlots = kRowB ? 8 : 1;
+    uint8_t a[kStages][A_BYTES];
+    uint8_t b[kStages][B_BYTES];
+    uint8_t out[EPI_WARPS][32 * 128];   // per promotion warp: 32 rows x 128 B, 128-byte swizzle
+    float sb[kSlots][BN];
+    uint64_t full[kStages];
+    uint64_t empty[kStages];
     uint64_t tfull[2];
     uint64_t tempty[2];
-    uint64_t sfull[SLOTS];
-    uint64_t sempty[SLOTS];
+    uint64_t sfull[kSlots];
+    uint64_t sempty[kSlots];
     uint64_t drain;
     uint32_t tmem_base;
     int abort_flag;
-    int bad_offsets;
 };
 
-constexpr size_t kSmemBytes = sizeof(Smem) + 1024;  // + alignment slack of the dynamic buffer
+template <int kRowB>
+constexpr size_t smem_bytes() {
+    return sizeof(Smem<kRowB>) + 1024;   // + alignment slack of the dynamic buffer
+}
+static_assert(smem_bytes<0>() <= 232448 && smem_bytes<1>() <= 232448, "shared memory per CTA");
 
 struct Params {
     const float* sa;
@@ -164,8 +176,9 @@ FP8FG_DEV uint32_t pack_bf16x2(float lo, float hi) {
 // ------------------------------------------------------------ producer ---
 // kRowB: B scales per row of B per K chunk (1) or per 128x128 block (0).
 template <int kRowB>
-FP8FG_DEV void run_producer(Smem& sm, const CUtensorMap* tmap_a, const CUtensorMap* tmap_b, const Params& p,
+FP8FG_DEV void run_producer(Smem<kRowB>& sm, const CUtensorMap* tmap_a, const CUtensorMap* tmap_b, const Params& p,
                             int64_t m_tiles, int64_t n_tiles, int64_t kb) {
+    constexpr int ST = Smem<kRowB>::kStages, SL = Smem<kRowB>::kSlots;
     volatile int* abort_flag = &sm.abort_flag;
     uint32_t g_ab = 0, g_sc = 0;  // chunks whose operand / scale copies were issued
     const int64_t num_tiles = m_tiles * n_tiles;
@@ -174,10 +187,9 @@ FP8FG_DEV void run_producer(Smem& sm, const CUtensorMap* tmap_a, const CUtensorM
         int64_t m0, n0;
         tile_origin(t, m_tiles, n_tiles, p.m_fastest, m0, n0);
         const int e = p.offsets ? expert_of(p.offsets, p.G, m0) : 0;
-        uint32_t sc_bytes = BM * 4;
-        if (kRowB) sc_bytes += static_cast<uint32_t>(min(static_cast<int64_t>(BN), p.N - n0) * 4);
+        const uint32_t sc_bytes = static_cast<uint32_t>(min(static_cast<int64_t>(BN), p.N - n0) * 4);
         for (int64_t c = 0; c < kb; ++c) {
-            const uint32_t s = g_ab % STAGES, ph = (g_ab / STAGES) & 1;
+            const uint32_t s = g_ab % ST, ph = (g_ab / ST) & 1;
             if (!mbar_wait_bounded(smem_u32(&sm.empty[s]), ph ^ 1, abort_flag, p.status, p.limit_ns, kErrTimeout)) {
                 ok = false;
                 break;
@@ -190,7 +202,8 @@ FP8FG_DEV void run_producer(Smem& sm, const CUtensorMap* tmap_a, const CUtensorM
             else
                 tma_load_2d(smem_u32(sm.b[s]), tmap_b, static_cast<int32_t>(c * BK), static_cast<int32_t>(n0), fb);
             ++g_ab;
-            const uint32_t sl = g_sc % SLOTS, sph = (g_sc / SLOTS) & 1;
+            if (!kRowB) continue;
+            const uint32_t sl = g_sc % SL, sph = (g_sc / SL) & 1;
             if (!mbar_wait_bounded(smem_u32(&sm.sempty[sl]), sph ^ 1, abort_flag, p.status, p.limit_ns,
                                    kErrTimeout)) {
                 ok = false;
@@ -198,34 +211,38 @@ FP8FG_DEV void run_producer(Smem& sm, const CUtensorMap* tmap_a, const CUtensorM
             }
             const uint32_t sfb = smem_u32(&sm.sfull[sl]);
             mbar_arrive_expect_tx(sfb, sc_bytes);
-            bulk_load(smem_u32(sm.sa[sl]), p.sa + c * p.M + m0, BM * 4, sfb);
-            if (kRowB) bulk_load(smem_u32(sm.sb[sl]), p.sb + c * p.N + n0, sc_bytes - BM * 4, sfb);
+            bulk_load(smem_u32(sm.sb[sl]), p.sb + c * p.N + n0, sc_bytes, sfb);
             ++g_sc;
         }
     }
     if (!ok) {
         // abort: let the copies already issued land before the CTA exits
-        for (uint32_t s = 0; s < STAGES && s < g_ab; ++s) {
-            const uint32_t last = s + STAGES * ((g_ab - 1 - s) / STAGES);
-            wait_plain(smem_u32(&sm.full[s]), (last / STAGES) & 1, 10000000ull);
+        for (uint32_t s = 0; s < ST && s < g_ab; ++s) {
+            const uint32_t last = s + ST * ((g_ab - 1 - s) / ST);
+            wait_plain(smem_u32(&sm.full[s]), (last / ST) & 1, 10000000ull);
         }
-        for (uint32_t s = 0; s < SLOTS && s < g_sc; ++s) {
-            const uint32_t last = s + SLOTS * ((g_sc - 1 - s) / SLOTS);
-            wait_plain(smem_u32(&sm.sfull[s]), (last / SLOTS) & 1, 10000000ull);
+        for (uint32_t s = 0; s < SL && s < g_sc; ++s) {
+            const uint32_t last = s + SL * ((g_sc - 1 - s) / SL);
+            wait_plain(smem_u32(&sm.sfull[s]), (last / SL) & 1, 10000000ull);
         }
     }
 }
 
 // ----------------------------------------------------------------- MMA ---
-FP8FG_DEV void run_mma(Smem& sm, uint32_t tmem_base, const Params& p, int64_t m_tiles, int64_t n_tiles, int64_t kb) {
+template <int kRowB>
+FP8FG_DEV void run_mma(Smem<kRowB>& sm, uint32_t tmem_base, const Params& p, int64_t m_tiles, int64_t n_tiles,
+                       int64_t kb) {
+    constexpr int ST = Smem<kRowB>::kStages;
     volatile int* abort_flag = &sm.abort_flag;
     uint32_t g = 0;
     const int64_t num_tiles = m_tiles * n_tiles;
     bool ok = true;
     for (int64_t t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
         for (int64_t c = 0; c < kb; ++c, ++g) {
-            const uint32_t s = g % STAGES, ph = (g / STAGES) & 1;
+            const uint32_t s = g % ST, ph = (g / ST) & 1;
             const uint32_t buf = g & 1, tph = (g >> 1) & 1;
+            // the promotion warps have read chunk g-2 out of this buffer, and
+            // the operands of chunk g have landed
             if (!mbar_wait_bounded(smem_u32(&sm.tempty[buf]), tph ^ 1, abort_flag, p.status, p.limit_ns,
                                    kErrTimeout) ||
                 !mbar_wait_bounded(smem_u32(&sm.full[s]), ph, abort_flag, p.status, p.limit_ns, kErrTimeout)) {
@@ -251,15 +268,32 @@ FP8FG_DEV void run_mma(Smem& sm, uint32_t tmem_base, const Params& p, int64_t m_
     wait_plain(smem_u32(&sm.drain), 0, 100000000ull);
 }
 
-// ------------------------------------------------------------ epilogue ---
+// ------------------------------------------------------------ promotion ---
+// acc[0..31] += P[0..31] * scale (block B scales) or
+// acc[0..31] += (P[0..31] * sbrow[0..31]) * sa (per-row B scales).
 template <int kRowB>
-FP8FG_DEV void run_epilogue(Smem& sm, uint32_t tmem_base, const Params& p, int64_t m_tiles, int64_t n_tiles,
-                            int64_t kb, int warp, int lane) {
+FP8FG_DEV void promote32(float* acc, const uint32_t (&r)[32], float scale, const float* sbrow) {
+#pragma unroll
+    for (int k = 0; k < 32; k += 2) {
+        float x0 = __uint_as_float(r[k]), x1 = __uint_as_float(r[k + 1]);
+        if (kRowB) {
+            const float2 s2 = *reinterpret_cast<const float2*>(sbrow + k);
+            mul2(x0, x1, s2.x, s2.y);
+        }
+        fma2(acc[k], acc[k + 1], x0, x1, scale, scale);
+    }
+}
+
+template <int kRowB>
+FP8FG_DEV void run_epilogue(Smem<kRowB>& sm, uint32_t tmem_base, const Params& p, const CUtensorMap* tmap_d,
+                            int64_t m_tiles, int64_t n_tiles, int64_t kb, int warp, int lane) {
+    constexpr int SL = Smem<kRowB>::kSlots;
     volatile int* abort_flag = &sm.abort_flag;
     const int quad = warp & 3;          // TMEM lanes this warp may read: 32*quad .. 32*quad+31
     const int half = (warp - 4) >> 2;   // columns 128*half .. 128*half+127 of the tile
     const int row = quad * 32 + lane;   // tile row owned by this thread
     const uint32_t t_lane = static_cast<uint32_t>(quad * 32) << 16;
+    const uint32_t ob = smem_u32(sm.out[warp - 4]);
     const int64_t num_tiles = m_tiles * n_tiles;
     uint32_t g = 0;
     for (int64_t t = blockIdx.x; t < num_tiles; t += gridDim.x) {
@@ -269,97 +303,133 @@ FP8FG_DEV void run_epilogue(Smem& sm, uint32_t tmem_base, const Params& p, int64
         const bool active = col0 < p.N;
         // block-mode B scales: lane l holds the scale of chunk 32*batch + l
         const float* sbp = p.sb;
+        float sb_cur = 0.0f, sb_nxt = 0.0f;
         if (!kRowB) {
             const int e = p.offsets ? expert_of(p.offsets, p.G, m0) : 0;
             sbp = p.sb + e * p.sb_group_stride + (col0 / 128) * p.sb_stride_n;
+            if (active && lane < kb) sb_cur = __ldg(sbp + lane * p.sb_stride_k);
+            if (active && lane + 32 < kb) sb_nxt = __ldg(sbp + (lane + 32) * p.sb_stride_k);
         }
-        float sb_cur = 0.0f, sb_nxt = 0.0f;
-        if (!kRowB && active) {
-            if (lane < kb) sb_cur = __ldg(sbp + lane * p.sb_stride_k);
-            if (lane + 32 < kb) sb_nxt = __ldg(sbp + (lane + 32) * p.sb_stride_k);
-        }
+        // A scales of chunks c, c+1, c+2 in flight
+        const float* sap = p.sa + m0 + row;
+        float q0 = __ldg(sap);
+        float q1 = kb > 1 ? __ldg(sap + p.M) : 0.0f;
+        float q2 = kb > 2 ? __ldg(sap + 2 * p.M) : 0.0f;
         float acc[128];
 #pragma unroll
         for (int j = 0; j < 128; ++j) acc[j] = 0.0f;
         for (int64_t c = 0; c < kb; ++c, ++g) {
             const uint32_t buf = g & 1, tph = (g >> 1) & 1;
-            const uint32_t sl = g % SLOTS, sph = (g / SLOTS) & 1;
+            const uint32_t sl = g % SL, sph = (g / SL) & 1;
             if (!kRowB && c > 0 && (c & 31) == 0) {
                 sb_cur = sb_nxt;
                 sb_nxt = (active && c + 32 + lane < kb) ? __ldg(sbp + (c + 32 + lane) * p.sb_stride_k) : 0.0f;
             }
+            const float sa_i = q0;
+            q0 = q1;
+            q1 = q2;
+            q2 = c + 3 < kb ? __ldg(sap + (c + 3) * p.M) : 0.0f;
             // every lane waits (each gets the barrier's acquire); the verdict
             // is made warp-uniform before any warp-collective instruction
             bool ok = mbar_wait_bounded(smem_u32(&sm.tfull[buf]), tph, abort_flag, p.status, p.limit_ns, kErrTimeout);
-            ok = ok && mbar_wait_bounded(smem_u32(&sm.sfull[sl]), sph, abort_flag, p.status, p.limit_ns, kErrTimeout);
-            if (!__all_sync(0xffffffffu, ok)) return;
+            if (kRowB)
+                ok = ok && mbar_wait_bounded(smem_u32(&sm.sfull[sl]), sph, abort_flag, p.status, p.limit_ns, kErrTimeout);
+            if (!__all_sync(0xffffffffu, ok)) {
+                // abort: the stores issued so far complete before the exit
+                if (lane == 0) bulk_wait_group0();
+                __syncwarp();
+                return;
+            }
             tc_fence_after();
-            const float sa_i = sm.sa[sl][row];
             const float sbv = __shfl_sync(0xffffffffu, sb_cur, static_cast<int>(c & 31));
             if (active) {
                 const uint32_t taddr = tmem_base + t_lane + buf * BN + 128 * half;
-                if (!kRowB) {
-                    const float scale = sa_i * sbv;
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        uint32_t r[32];
-                        tmem_ld_32x32b_x32(taddr + 32 * j, r);
-                        tmem_ld_wait();
-#pragma unroll
-                        for (int k = 0; k < 32; ++k) acc[32 * j + k] = fmaf(__uint_as_float(r[k]), scale, acc[32 * j + k]);
-                    }
-                } else {
-                    const float* sbrow = sm.sb[sl] + 128 * half;
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        uint32_t r[32];
-                        tmem_ld_32x32b_x32(taddr + 32 * j, r);
-                        tmem_ld_wait();
-#pragma unroll
-                        for (int k = 0; k < 32; ++k)
-                            acc[32 * j + k] = fmaf(__uint_as_float(r[k]) * sbrow[32 * j + k], sa_i, acc[32 * j + k]);
-                    }
-                }
+                const float scale = kRowB ? sa_i : sa_i * sbv;
+                const float* sbrow = sm.sb[sl] + 128 * half;
+                // 4 x 32 columns; the next load is in flight while the
+                // previous 32 columns are folded in
+                uint32_t ra[32], rb[32];
+                tmem_ld_32x32b_x32(taddr, ra);
+                tmem_ld_wait(ra);
+                tmem_ld_32x32b_x32(taddr + 32, rb);
+                promote32<kRowB>(acc, ra, scale, sbrow);
+                tmem_ld_wait(rb);
+                tmem_ld_32x32b_x32(taddr + 64, ra);
+                promote32<kRowB>(acc + 32, rb, scale, sbrow + 32);
+                tmem_ld_wait(ra);
+                tmem_ld_32x32b_x32(taddr + 96, rb);
+                promote32<kRowB>(acc + 64, ra, scale, sbrow + 64);
+                tmem_ld_wait(rb);
+                promote32<kRowB>(acc + 96, rb, scale, sbrow + 96);
             }
+            // the buffer goes back only after the loaded registers are consumed
             tc_fence_before();
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(smem_u32(&sm.tempty[buf]));
-                mbar_arrive(smem_u32(&sm.sempty[sl]));
+                if (kRowB) mbar_arrive(smem_u32(&sm.sempty[sl]));
             }
         }
         if (!active) continue;
+        // 32 rows x 128 columns of this warp -> shared memory (row = lane,
+        // 16-byte chunk k of each 128-byte row at k ^ (row & 7): the 128-byte
+        // swizzle of the output map) -> one TMA store per 128 bytes of row
+        const uint32_t orow = ob + static_cast<uint32_t>(lane) * 128;
+        const int32_t gy = static_cast<int32_t>(m0 + quad * 32);
         if (p.out_bf16) {
-            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.d) + (m0 + row) * p.N + col0);
 #pragma unroll
-            for (int v = 0; v < 16; ++v) {
-                uint4 o;
-                o.x = pack_bf16x2(acc[8 * v + 0], acc[8 * v + 1]);
-                o.y = pack_bf16x2(acc[8 * v + 2], acc[8 * v + 3]);
-                o.z = pack_bf16x2(acc[8 * v + 4], acc[8 * v + 5]);
-                o.w = pack_bf16x2(acc[8 * v + 6], acc[8 * v + 7]);
-                dst[v] = o;
+            for (int rd = 0; rd < 2; ++rd) {
+                if (lane == 0) bulk_wait_group_read0();   // the previous store has read the buffer
+                __syncwarp();
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const float* a8 = acc + 64 * rd + 8 * k;
+                    st_shared_v4(orow + ((k ^ (lane & 7)) << 4), pack_bf16x2(a8[0], a8[1]), pack_bf16x2(a8[2], a8[3]),
+                                 pack_bf16x2(a8[4], a8[5]), pack_bf16x2(a8[6], a8[7]));
+                }
+                fence_proxy_async_shared();
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_2d(tmap_d, ob, static_cast<int32_t>(col0 + 64 * rd), gy);
+                    bulk_commit_group();
+                }
             }
         } else {
-            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.d) + (m0 + row) * p.N + col0);
 #pragma unroll
-            for (int v = 0; v < 32; ++v)
-                dst[v] = make_float4(acc[4 * v + 0], acc[4 * v + 1], acc[4 * v + 2], acc[4 * v + 3]);
+            for (int rd = 0; rd < 4; ++rd) {
+                if (lane == 0) bulk_wait_group_read0();
+                __syncwarp();
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const float* a4 = acc + 32 * rd + 4 * k;
+                    st_shared_v4(orow + ((k ^ (lane & 7)) << 4), __float_as_uint(a4[0]), __float_as_uint(a4[1]),
+                                 __float_as_uint(a4[2]), __float_as_uint(a4[3]));
+                }
+                fence_proxy_async_shared();
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_2d(tmap_d, ob, static_cast<int32_t>(col0 + 32 * rd), gy);
+                    bulk_commit_group();
+                }
+            }
         }
     }
+    if (lane == 0) bulk_wait_group0();   // every store of this warp has completed
+    __syncwarp();
 }
 
 template <int kRowB>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_blockscaled_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
-                            const Params p) {
+                            const __grid_constant__ CUtensorMap tmap_d, const Params p) {
+    using S = Smem<kRowB>;
     extern __shared__ uint8_t smem_raw[];
-    Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    S& sm = *reinterpret_cast<S*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t m_tiles = p.M / BM, n_tiles = (p.N + BN - 1) / BN, kb = p.K / BK;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
+        for (int s = 0; s < S::kStages; ++s) {
             mbar_init(smem_u32(&sm.full[s]), 1);
             mbar_init(smem_u32(&sm.empty[s]), 1);
         }
@@ -367,18 +437,18 @@ __global__ void __launch_bounds__(THREADS, 1)
             mbar_init(smem_u32(&sm.tfull[b]), 1);
             mbar_init(smem_u32(&sm.tempty[b]), EPI_WARPS);
         }
-        for (int s = 0; s < SLOTS; ++s) {
+        for (int s = 0; s < S::kSlots; ++s) {
             mbar_init(smem_u32(&sm.sfull[s]), 1);
             mbar_init(smem_u32(&sm.sempty[s]), EPI_WARPS);
         }
         mbar_init(smem_u32(&sm.drain), 1);
         sm.abort_flag = 0;
-        sm.bad_offsets = 0;
         fence_barrier_init();
     }
     if (warp == 0 && lane == 0) {
         prefetch_tensormap(&tmap_a);
         prefetch_tensormap(&tmap_b);
+        prefetch_tensormap(&tmap_d);
     }
     if (warp == 1) tmem_alloc(smem_u32(&sm.tmem_base), TMEM_COLS);
     int bad = 0;
@@ -402,10 +472,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     } else if (warp < 4) {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(REGS_LOW));
         if (warp == 0 && lane == 0) run_producer<kRowB>(sm, &tmap_a, &tmap_b, p, m_tiles, n_tiles, kb);
-        if (warp == 1 && lane == 0) run_mma(sm, tmem_base, p, m_tiles, n_tiles, kb);
+        if (warp == 1 && lane == 0) run_mma<kRowB>(sm, tmem_base, p, m_tiles, n_tiles, kb);
     } else {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(REGS_HIGH));
-        run_epilogue<kRowB>(sm, tmem_base, p, m_tiles, n_tiles, kb, warp, lane);
+        run_epilogue<kRowB>(sm, tmem_base, p, &tmap_d, m_tiles, n_tiles, kb, warp, lane);
     }
     __syncwarp();
     tc_fence_before();
@@ -446,6 +516,22 @@ bool encode_operand_map(CUtensorMap* map, const void* base, int64_t rows, int64_
     return r == CUDA_SUCCESS;
 }
 
+// Output map over D [M, N] (BF16 or FP32): box of 128 bytes of a row x 32
+// rows, 128-byte swizzle (the promotion warps' staging layout).
+bool encode_output_map(CUtensorMap* map, void* base, int64_t M, int64_t N, bool bf16) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = get_encode_fn();
+    if (!enc) return false;
+    const cuuint64_t esz = bf16 ? 2 : 4;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(M)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(N) * esz};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / esz), 32};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims,
+                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 std::once_flag g_attr_once[64];
 
 }  // namespace
@@ -458,21 +544,23 @@ int launch_gemm(const GemmArgs& a, int num_sms, int* status_word, cudaStream_t s
         cudaError_t e = cudaSuccess;
         std::call_once(g_attr_once[dev], [&] {
             e = cudaFuncSetAttribute(gemm_blockscaled_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     static_cast<int>(kSmemBytes));
+                                     static_cast<int>(smem_bytes<0>()));
             if (e == cudaSuccess)
                 e = cudaFuncSetAttribute(gemm_blockscaled_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(kSmemBytes));
+                                         static_cast<int>(smem_bytes<1>()));
         });
         if (e != cudaSuccess) {
             *cuda_err = e;
             return kErrCuda;
         }
     }
-    CUtensorMap tmap_a, tmap_b;
+    CUtensorMap tmap_a, tmap_b, tmap_d;
     std::memset(&tmap_a, 0, sizeof tmap_a);
     std::memset(&tmap_b, 0, sizeof tmap_b);
+    std::memset(&tmap_d, 0, sizeof tmap_d);
     if (!encode_operand_map(&tmap_a, a.a, a.M, a.K, 0, BM)) return kErrCuda;
     if (!encode_operand_map(&tmap_b, a.b, a.N, a.K, a.offsets ? a.G : 0, BN)) return kErrCuda;
+    if (!encode_output_map(&tmap_d, a.d, a.M, a.N, a.out_bf16 != 0)) return kErrCuda;
     Params p;
     p.sa = a.sa;
     p.sb = a.sb;
@@ -494,9 +582,11 @@ int launch_gemm(const GemmArgs& a, int num_sms, int* status_word, cudaStream_t s
     const int64_t grid = tiles < num_sms ? tiles : num_sms;
     if (grid <= 0) return kOk;
     if (a.bscale == 1)
-        gemm_blockscaled_kernel<1><<<static_cast<unsigned>(grid), THREADS, kSmemBytes, stream>>>(tmap_a, tmap_b, p);
+        gemm_blockscaled_kernel<1><<<static_cast<unsigned>(grid), THREADS, smem_bytes<1>(), stream>>>(tmap_a, tmap_b,
+                                                                                                      tmap_d, p);
     else
-        gemm_blockscaled_kernel<0><<<static_cast<unsigned>(grid), THREADS, kSmemBytes, stream>>>(tmap_a, tmap_b, p);
+        gemm_blockscaled_kernel<0><<<static_cast<unsigned>(grid), THREADS, smem_bytes<0>(), stream>>>(tmap_a, tmap_b,
+                                                                                                      tmap_d, p);
     *cuda_err = cudaPeekAtLastError();
     return *cuda_err == cudaSuccess ? kOk : kErrCuda;
 }

@@ -1,6 +1,7 @@
-// ptx.cuh -- thin inline-PTX wrappers for sm_103a: mbarriers, TMA (tensor and
-// bulk copies), tcgen05 (TMEM allocation, MMA, commit, loads, fences), the
-// E4M3 conversion and the global timer.  Written from the PTX ISA; no
+// ptx.cuh -- thin inline-PTX wrappers for sm_103a: mbarriers, named
+// barriers, TMA (tensor loads and stores, bulk copies), tcgen05 (TMEM
+// allocation, MMA, commit, loads, fences), packed FP32 arithmetic, the E4M3
+// conversion and the global timer.  Written from the PTX ISA; no
 // library headers beyond the CUDA runtime.
 #pragma once
 #include <cstdint>
@@ -71,6 +72,20 @@ FP8FG_DEV bool mbar_wait_bounded(uint32_t bar, uint32_t parity, volatile int* ab
     }
 }
 
+// ------------------------------------------------------- named barriers ---
+// bar.arrive / bar.sync on hardware barrier `id` (1..15; 0 is __syncthreads)
+// completing when `kThreads` threads (whole warps) have arrived.  bar.sync
+// blocks without a time limit: every user keeps the arrival count exact on
+// all paths, including aborts.
+template <int kThreads>
+FP8FG_DEV void named_arrive(int id) {
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "n"(kThreads) : "memory");
+}
+template <int kThreads>
+FP8FG_DEV void named_sync(int id) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "n"(kThreads) : "memory");
+}
+
 // ----------------------------------------------------------------- TMA ---
 
 FP8FG_DEV void tma_load_2d(uint32_t dst, const CUtensorMap* map, int32_t x, int32_t y, uint32_t bar) {
@@ -95,6 +110,26 @@ FP8FG_DEV void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
                  "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
                  : "memory");
+}
+
+// Tiled store shared -> global of one box at (x, y), tracked by this
+// thread's bulk async-group.
+FP8FG_DEV void tma_store_2d(const CUtensorMap* map, uint32_t src, int32_t x, int32_t y) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(src), "r"(x), "r"(y)
+                 : "memory");
+}
+FP8FG_DEV void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// this thread's bulk stores have finished reading shared memory
+FP8FG_DEV void bulk_wait_group_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// this thread's bulk stores have completed
+FP8FG_DEV void bulk_wait_group0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// generic-proxy shared-memory writes -> visible to the async proxy (TMA)
+FP8FG_DEV void fence_proxy_async_shared() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+FP8FG_DEV void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
 FP8FG_DEV void prefetch_tensormap(const CUtensorMap* map) {
@@ -149,6 +184,30 @@ FP8FG_DEV void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32]) {
 }
 
 FP8FG_DEV void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// tcgen05.wait::ld that also marks the loaded registers as written there, so
+// no use of them can be scheduled before the wait.
+FP8FG_DEV void tmem_ld_wait(uint32_t (&r)[32]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int k = 0; k < 32; ++k) asm volatile("" : "+r"(r[k]));
+}
+
+// --------------------------------------------------- packed FP32 (x2) ---
+// Two IEEE binary32 operations per instruction, each lane rounded to
+// nearest even exactly as the scalar fmaf / multiplication.
+FP8FG_DEV void fma2(float& a0, float& a1, float x0, float x1, float s0, float s1) {
+    asm("{\n\t.reg .b64 A, X, S;\n\tmov.b64 A, {%0, %1};\n\tmov.b64 X, {%2, %3};\n\tmov.b64 S, {%4, %5};\n\t"
+        "fma.rn.f32x2 A, X, S, A;\n\tmov.b64 {%0, %1}, A;\n\t}"
+        : "+f"(a0), "+f"(a1)
+        : "f"(x0), "f"(x1), "f"(s0), "f"(s1));
+}
+FP8FG_DEV void mul2(float& x0, float& x1, float s0, float s1) {
+    asm("{\n\t.reg .b64 X, S;\n\tmov.b64 X, {%0, %1};\n\tmov.b64 S, {%2, %3};\n\t"
+        "mul.rn.f32x2 X, X, S;\n\tmov.b64 {%0, %1}, X;\n\t}"
+        : "+f"(x0), "+f"(x1)
+        : "f"(s0), "f"(s1));
+}
 
 // ---------------------------------------------------------------- E4M3 ---
 
