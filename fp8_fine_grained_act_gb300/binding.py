@@ -45,6 +45,7 @@ SIGNATURES = {
     "fp8fg_status_string": (ctypes.c_char_p, [_i32]),
     "fp8fg_last_device_status": (_i32, [_vp]),
     "fp8fg_selftest_watchdog": (_i32, [_i64, _vp]),
+    "fp8fg_set_wait_limit": (_i32, [_i64]),
 }
 
 
@@ -206,6 +207,11 @@ def fp8fg_last_device_status(stream=None) -> int:
 
 def fp8fg_selftest_watchdog(timeout_ns: int, stream=None) -> int:
     return int(load().fp8fg_selftest_watchdog(int(timeout_ns), _stream(stream)))
+
+
+def fp8fg_set_wait_limit(limit_ns: int) -> int:
+    """Limit of the GEMM kernels' bounded waits (0: the 2 s default)."""
+    return int(load().fp8fg_set_wait_limit(int(limit_ns)))
 
 
 def fp8fg_status_string(status: int) -> str:

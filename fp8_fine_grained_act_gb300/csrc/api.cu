@@ -2,6 +2,7 @@
 // the library-owned device status word, and dispatch to the kernels.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 #include <mutex>
 
@@ -24,6 +25,7 @@ struct DeviceInfo {
 };
 
 DeviceInfo g_dev[kMaxDevices];
+std::atomic<uint64_t> g_wait_limit_ns{kWaitLimitNs};
 std::mutex g_dev_mu;
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -104,7 +106,9 @@ static int gemm_common(const GemmArgs& a, cudaStream_t stream) {
         return from_cuda(cudaMemsetAsync(a.d, 0, static_cast<size_t>(a.M) * a.N * elt, stream));
     }
     cudaError_t ce = cudaSuccess;
-    return launch_gemm(a, d->num_sms, d->status_word, stream, &ce);
+    GemmArgs b = a;
+    b.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
+    return launch_gemm(b, d->num_sms, d->status_word, stream, &ce);
 }
 
 // Shape rules shared by the dense and grouped GEMMs.  TMA addresses rows of
@@ -205,6 +209,12 @@ int fp8fg_last_device_status(cudaStream_t stream) {
         cudaStreamSynchronize(stream) != cudaSuccess)
         return kErrCuda;
     return value;
+}
+
+int fp8fg_set_wait_limit(int64_t limit_ns) {
+    if (limit_ns < 0 || static_cast<uint64_t>(limit_ns) > kMaxWaitLimitNs) return kErrInvalidArg;
+    g_wait_limit_ns.store(limit_ns == 0 ? kWaitLimitNs : static_cast<uint64_t>(limit_ns), std::memory_order_relaxed);
+    return kOk;
 }
 
 int fp8fg_selftest_watchdog(int64_t timeout_ns, cudaStream_t stream) {

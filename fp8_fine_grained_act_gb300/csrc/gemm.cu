@@ -22,14 +22,17 @@
 //               swizzle), plus,
 //               for per-row B scales, the chunk's 256 B scales into a ring
 //               of their own; everything completes on mbarriers;
-//   warp 1      MMA issuer: 4 x tcgen05.mma.kind::f8f6f4 (K = 32 each) per
-//               chunk into one of two 256-column TMEM buffers, then commits
-//               to the stage's "empty" mbarrier and the buffer's "full" one;
+//   warp 1      MMA issuer (lane 0 issues, the warp waits): before reusing a
+//               TMEM buffer it takes the buffer back from the promotion
+//               warps on a named barrier (bar.sync), then 4 x
+//               tcgen05.mma.kind::f8f6f4 (K = 32 each) per chunk into one of
+//               two 256-column buffers, and commits to the stage's "empty"
+//               mbarrier and the buffer's "full" one;
 //   warps 2-3   idle;
 //   warps 4-11  promotion: wait for the buffer, tcgen05.ld 4 x 32 columns
 //               (the next load in flight while the previous 32 columns are
 //               scaled and added with packed FP32 FMAs), hand the buffer
-//               back (mbarrier), and after the tile's last chunk write the 128 x 256
+//               back (bar.arrive), and after the tile's last chunk write the 128 x 256
 //               outputs through shared memory with TMA stores.  The A scales
 //               come straight from global memory, three chunks ahead, into
 //               registers; block B scales come 32 chunks per load, one per
@@ -62,6 +65,13 @@ constexpr int REGS_LOW = 64, REGS_HIGH = 216;
 constexpr uint32_t TMEM_COLS = 2 * BN;
 constexpr uint32_t A_BYTES = BM * BK;
 constexpr uint32_t B_BYTES = BN * BK;
+// Named barriers 1 and 2: the 8 promotion warps hand TMEM buffer b back to
+// the MMA warp through barrier 1 + b (bar.arrive by them, bar.sync by the
+// whole MMA warp).
+constexpr int kRelThreads = 32 * (1 + EPI_WARPS);
+// Limit of the promotion warps' wait for a chunk's commit (see run_epilogue):
+// far above the longest settable limit of the other waits.
+constexpr uint64_t kHandoffLimitNs = 3 * kMaxWaitLimitNs;
 
 // Shared memory.  kRowB = 1 (B scales per row of B) also keeps a ring of
 // the chunks' B scales.  (Three operand stages measured faster than four on
@@ -77,7 +87,6 @@ struct __align__(1024) Smem {
     uint64_t full[kStages];
     uint64_t empty[kStages];
     uint64_t tfull[2];
-    uint64_t tempty[2];
     uint64_t sfull[kSlots];
     uint64_t sempty[kSlots];
     uint64_t drain;
@@ -229,43 +238,60 @@ FP8FG_DEV void run_producer(Smem<kRowB>& sm, const CUtensorMap* tmap_a, const CU
 }
 
 // ----------------------------------------------------------------- MMA ---
+// Whole warp; lane 0 issues.  Lock step with the promotion warps: before
+// chunk g (g >= 2) the warp takes the hand-back of chunk g-2 on the named
+// barrier of its buffer, and for every chunk, aborted or not, lane 0 commits
+// the buffer's "full" mbarrier (with no MMA after an abort the commit only
+// tracks the earlier ones).  A promotion warp arrives for chunk g only after
+// that commit, so no arrival can run ahead of the MMA warp's bar.sync, and
+// every bar.sync is matched by the 8 arrivals of a chunk already committed.
 template <int kRowB>
 FP8FG_DEV void run_mma(Smem<kRowB>& sm, uint32_t tmem_base, const Params& p, int64_t m_tiles, int64_t n_tiles,
-                       int64_t kb) {
+                       int64_t kb, int lane) {
     constexpr int ST = Smem<kRowB>::kStages;
     volatile int* abort_flag = &sm.abort_flag;
     uint32_t g = 0;
     const int64_t num_tiles = m_tiles * n_tiles;
-    bool ok = true;
-    for (int64_t t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
+    bool ok = true;   // warp-uniform
+    for (int64_t t = blockIdx.x; t < num_tiles; t += gridDim.x) {
         for (int64_t c = 0; c < kb; ++c, ++g) {
             const uint32_t s = g % ST, ph = (g / ST) & 1;
-            const uint32_t buf = g & 1, tph = (g >> 1) & 1;
-            // the promotion warps have read chunk g-2 out of this buffer, and
-            // the operands of chunk g have landed
-            if (!mbar_wait_bounded(smem_u32(&sm.tempty[buf]), tph ^ 1, abort_flag, p.status, p.limit_ns,
-                                   kErrTimeout) ||
-                !mbar_wait_bounded(smem_u32(&sm.full[s]), ph, abort_flag, p.status, p.limit_ns, kErrTimeout)) {
-                ok = false;
-                break;
+            const uint32_t buf = g & 1;
+            if (g >= 2) named_sync<kRelThreads>(1 + static_cast<int>(buf));
+            if (ok) {
+                bool f = true;
+                if (lane == 0)
+                    f = mbar_wait_bounded(smem_u32(&sm.full[s]), ph, abort_flag, p.status, p.limit_ns, kErrTimeout);
+                ok = __shfl_sync(0xffffffffu, f, 0) != 0;
             }
-            tc_fence_after();
-            const uint32_t d_tmem = tmem_base + buf * BN;
-            const uint64_t adesc = smem_desc_sw128(smem_u32(sm.a[s]));
-            const uint64_t bdesc = smem_desc_sw128(smem_u32(sm.b[s]));
+            if (lane == 0) {
+                if (ok) {
+                    tc_fence_after();
+                    const uint32_t d_tmem = tmem_base + buf * BN;
+                    const uint64_t adesc = smem_desc_sw128(smem_u32(sm.a[s]));
+                    const uint64_t bdesc = smem_desc_sw128(smem_u32(sm.b[s]));
 #pragma unroll
-            for (int kk = 0; kk < BK / MMA_K; ++kk) {
-                // advance 32 bytes along K inside the 128-byte swizzle atom
-                const uint64_t koff = static_cast<uint64_t>((kk * MMA_K) >> 4);
-                mma_f8f6f4(d_tmem, adesc + koff, bdesc + koff, kIdesc, kk > 0 ? 1u : 0u);
+                    for (int kk = 0; kk < BK / MMA_K; ++kk) {
+                        // advance 32 bytes along K inside the 128-byte swizzle atom
+                        const uint64_t koff = static_cast<uint64_t>((kk * MMA_K) >> 4);
+                        mma_f8f6f4(d_tmem, adesc + koff, bdesc + koff, kIdesc, kk > 0 ? 1u : 0u);
+                    }
+                    mma_commit(smem_u32(&sm.empty[s]));
+                }
+                mma_commit(smem_u32(&sm.tfull[buf]));
             }
-            mma_commit(smem_u32(&sm.empty[s]));
-            mma_commit(smem_u32(&sm.tfull[buf]));
+            __syncwarp();
         }
     }
-    // every MMA issued by this thread has finished before TMEM is released
-    mma_commit(smem_u32(&sm.drain));
-    wait_plain(smem_u32(&sm.drain), 0, 100000000ull);
+    // the last hand-back of each buffer that was used
+    for (uint32_t b = 0; b < 2; ++b)
+        if (g > b) named_sync<kRelThreads>(1 + static_cast<int>(b));
+    if (lane == 0) {
+        // every MMA issued by this thread has finished before TMEM is released
+        mma_commit(smem_u32(&sm.drain));
+        wait_plain(smem_u32(&sm.drain), 0, 100000000ull);
+    }
+    __syncwarp();
 }
 
 // ------------------------------------------------------------ promotion ---
@@ -296,6 +322,8 @@ FP8FG_DEV void run_epilogue(Smem<kRowB>& sm, uint32_t tmem_base, const Params& p
     const uint32_t ob = smem_u32(sm.out[warp - 4]);
     const int64_t num_tiles = m_tiles * n_tiles;
     uint32_t g = 0;
+    bool dead = false;   // after a failed wait: no work, but still one hand-back per chunk
+    bool timed_out = false;
     for (int64_t t = blockIdx.x; t < num_tiles; t += gridDim.x) {
         int64_t m0, n0;
         tile_origin(t, m_tiles, n_tiles, p.m_fastest, m0, n0);
@@ -329,20 +357,28 @@ FP8FG_DEV void run_epilogue(Smem<kRowB>& sm, uint32_t tmem_base, const Params& p
             q0 = q1;
             q1 = q2;
             q2 = c + 3 < kb ? __ldg(sap + (c + 3) * p.M) : 0.0f;
-            // every lane waits (each gets the barrier's acquire); the verdict
-            // is made warp-uniform before any warp-collective instruction
-            bool ok = mbar_wait_bounded(smem_u32(&sm.tfull[buf]), tph, abort_flag, p.status, p.limit_ns, kErrTimeout);
-            if (kRowB)
-                ok = ok && mbar_wait_bounded(smem_u32(&sm.sfull[sl]), sph, abort_flag, p.status, p.limit_ns, kErrTimeout);
+            // Every lane waits (each gets the barrier's acquire).  The MMA
+            // warp commits this barrier for every chunk, aborted or not, so
+            // the wait ignores the abort flag; its limit is far above the
+            // longest wait the commit can depend on.
+            // (After such a wait has failed, which the lock step rules out,
+            // the later ones are kept short so the kernel still ends.)
+            bool ok = wait_plain(smem_u32(&sm.tfull[buf]), tph, timed_out ? 1000000ull : kHandoffLimitNs);
             if (!__all_sync(0xffffffffu, ok)) {
-                // abort: the stores issued so far complete before the exit
-                if (lane == 0) bulk_wait_group0();
-                __syncwarp();
-                return;
+                if (lane == 0) {
+                    atomicCAS(p.status, 0, kErrTimeout);
+                    *abort_flag = 1;
+                }
+                dead = true;
+                timed_out = true;
+            }
+            if (kRowB && !dead) {
+                ok = mbar_wait_bounded(smem_u32(&sm.sfull[sl]), sph, abort_flag, p.status, p.limit_ns, kErrTimeout);
+                if (!__all_sync(0xffffffffu, ok)) dead = true;
             }
             tc_fence_after();
             const float sbv = __shfl_sync(0xffffffffu, sb_cur, static_cast<int>(c & 31));
-            if (active) {
+            if (active && !dead) {
                 const uint32_t taddr = tmem_base + t_lane + buf * BN + 128 * half;
                 const float scale = kRowB ? sa_i : sa_i * sbv;
                 const float* sbrow = sm.sb[sl] + 128 * half;
@@ -364,13 +400,10 @@ FP8FG_DEV void run_epilogue(Smem<kRowB>& sm, uint32_t tmem_base, const Params& p
             }
             // the buffer goes back only after the loaded registers are consumed
             tc_fence_before();
-            __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(smem_u32(&sm.tempty[buf]));
-                if (kRowB) mbar_arrive(smem_u32(&sm.sempty[sl]));
-            }
+            named_arrive<kRelThreads>(1 + static_cast<int>(buf));
+            if (kRowB && !dead && lane == 0) mbar_arrive(smem_u32(&sm.sempty[sl]));
         }
-        if (!active) continue;
+        if (!active || dead) continue;
         // 32 rows x 128 columns of this warp -> shared memory (row = lane,
         // 16-byte chunk k of each 128-byte row at k ^ (row & 7): the 128-byte
         // swizzle of the output map) -> one TMA store per 128 bytes of row
@@ -433,10 +466,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             mbar_init(smem_u32(&sm.full[s]), 1);
             mbar_init(smem_u32(&sm.empty[s]), 1);
         }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(smem_u32(&sm.tfull[b]), 1);
-            mbar_init(smem_u32(&sm.tempty[b]), EPI_WARPS);
-        }
+        for (int b = 0; b < 2; ++b) mbar_init(smem_u32(&sm.tfull[b]), 1);
         for (int s = 0; s < S::kSlots; ++s) {
             mbar_init(smem_u32(&sm.sfull[s]), 1);
             mbar_init(smem_u32(&sm.sempty[s]), EPI_WARPS);
@@ -472,7 +502,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     } else if (warp < 4) {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(REGS_LOW));
         if (warp == 0 && lane == 0) run_producer<kRowB>(sm, &tmap_a, &tmap_b, p, m_tiles, n_tiles, kb);
-        if (warp == 1 && lane == 0) run_mma<kRowB>(sm, tmem_base, p, m_tiles, n_tiles, kb);
+        if (warp == 1) run_mma<kRowB>(sm, tmem_base, p, m_tiles, n_tiles, kb, lane);
     } else {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(REGS_HIGH));
         run_epilogue<kRowB>(sm, tmem_base, p, &tmap_d, m_tiles, n_tiles, kb, warp, lane);
@@ -577,7 +607,7 @@ int launch_gemm(const GemmArgs& a, int num_sms, int* status_word, cudaStream_t s
     p.G = a.G;
     p.m_fastest = a.offsets ? 0 : 1;
     p.status = status_word;
-    p.limit_ns = kWaitLimitNs;
+    p.limit_ns = a.wait_limit_ns;
     const int64_t tiles = (a.M / BM) * ((a.N + BN - 1) / BN);
     const int64_t grid = tiles < num_sms ? tiles : num_sms;
     if (grid <= 0) return kOk;

@@ -9,8 +9,10 @@ namespace fp8fg {
 // Library status codes (mirror fp8fg_status of the public header).
 enum : int { kOk = 0, kErrInvalidArg = 1, kErrMisaligned = 2, kErrUnsupported = 3, kErrCuda = 4, kErrTimeout = 5 };
 
-// Bounded device waits give up after this long (nanoseconds).
+// Bounded device waits give up after this long (nanoseconds) by default;
+// fp8fg_set_wait_limit() changes it within [1, kMaxWaitLimitNs].
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
+constexpr uint64_t kMaxWaitLimitNs = 10000000000ull;
 
 cudaError_t launch_quant_act_rows(const void* x, int64_t rows, int64_t cols, uint8_t* q, float* scales, int num_sms,
                                   cudaStream_t stream);
@@ -32,6 +34,7 @@ struct GemmArgs {
     int64_t M, N, K;
     const int32_t* offsets;   // grouped: device int32[G+1]; nullptr for a dense GEMM
     int G;
+    uint64_t wait_limit_ns;   // limit of the kernel's bounded waits
 };
 
 // Returns a library status code; `cuda_err` receives the CUDA error when the

@@ -172,6 +172,19 @@ const char *fp8fg_status_string(int status);
 int fp8fg_last_device_status(cudaStream_t stream);
 
 /*
+ * fp8fg_set_wait_limit -- limit, in nanoseconds, of the GEMM kernels' bounded
+ * waits on their producer and consumer barriers (TMA data, scale ring, MMA
+ * completion), for every later launch in this process on any device.
+ * 0 restores the default of 2 s; allowed range 0 .. 10^10.  A wait that runs
+ * out records FP8FG_ERR_TIMEOUT in the device status word and the kernel
+ * winds down without computing (its output is then undefined) and returns.
+ * A very short limit makes the waits run out on purpose (a test of those
+ * paths).  The pages describe no such control: it belongs to this library's
+ * failure detection.  Returns FP8FG_ERR_INVALID_ARG outside the range.
+ */
+int fp8fg_set_wait_limit(int64_t limit_ns);
+
+/*
  * fp8fg_selftest_watchdog -- test hook for the kernels' bounded waits: runs a
  * one-warp kernel that waits on an mbarrier nobody arrives on, with a limit
  * of `timeout_ns` nanoseconds (1 .. 10^9).  The wait gives up, records

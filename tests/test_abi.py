@@ -23,7 +23,8 @@ def _declared_functions():
 def test_header_declares_the_entry_points():
     names = _declared_functions()
     for n in ["fp8_quant_act_1x128", "fp8_quant_w_128x128", "fp8_gemm_blockscaled", "fp8_gemm_grouped",
-              "fp8fg_status_string", "fp8fg_last_device_status", "fp8fg_selftest_watchdog"]:
+              "fp8fg_status_string", "fp8fg_last_device_status", "fp8fg_selftest_watchdog",
+              "fp8fg_set_wait_limit"]:
         assert n in names
 
 
@@ -105,6 +106,14 @@ def test_gemm_argument_checks(lib):
 def test_watchdog_argument_checks(lib):
     assert lib.fp8fg_selftest_watchdog(0, None) == 1
     assert lib.fp8fg_selftest_watchdog(2_000_000_000, None) == 1
+
+
+def test_wait_limit_range(lib):
+    assert lib.fp8fg_set_wait_limit(-1) == 1
+    assert lib.fp8fg_set_wait_limit(10_000_000_001) == 1
+    assert lib.fp8fg_set_wait_limit(10_000_000_000) == 0
+    assert lib.fp8fg_set_wait_limit(1) == 0
+    assert lib.fp8fg_set_wait_limit(0) == 0             # back to the default
 
 
 def test_no_device_means_an_error_not_a_fallback(lib):
