@@ -44,6 +44,7 @@ WORKLOAD = ("Fprop linear: X[4096,7168] bf16 N(0,1) with 8 fixed outlier channel
 FLOPS = 2.0 * M * N * K
 ACT_BYTES = M * K * 2 + M * K + (K // 128) * M * 4                 # 3.031 B per element
 W_BYTES = N * K * 4 + N * K + (N // 128) * (K // 128) * 4         # 5.0002 B per element
+DUAL_BYTES = M * K * 2 + 2 * M * K + 2 * (K // 128) * M * 4        # 4.0625 B per element (one read, two outputs)
 GEMM_MIN_BYTES = M * K + N * K + 4 * (M * K // 128 + N * K // 16384) + M * N * 2
 FP8_OVER_BF16 = 4.5 / 2.25          # nominal dense FP8 : BF16 tensor ratio
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
@@ -301,6 +302,19 @@ def run_gpu(args):
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps)
 
+    # outside the step: the fused 1x128 + 128x1 quantizer on the same X (what a
+    # training forward runs to cache X in FP8 for the weight gradient)
+    qr, srw, qct, scl = fb.fp8_quant_act_dual(x, stream=stream)
+    dual_iters = 50
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(dual_iters):
+        fb.fp8_quant_act_dual(x, stream=stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    t_dual = max_over_ranks(e0.elapsed_time(e1) / dual_iters)
+    del qr, srw, qct, scl
+
     ms_step = max_over_ranks(total_ms / args.steps)
     t_gemm = max_over_ranks(t_gemm)
     t_act = max_over_ranks(t_act)
@@ -339,6 +353,9 @@ def run_gpu(args):
                                 "frac_hbm": ACT_BYTES / (t_act * 1e-3) / 1e9 / hbm},
             "quant_w_128x128": {"us": t_w * 1e3, "GB/s": W_BYTES / (t_w * 1e-3) / 1e9,
                                 "frac_hbm": W_BYTES / (t_w * 1e-3) / 1e9 / hbm},
+            "quant_act_dual_1x128_128x1 (not in the step)": {
+                "us": t_dual * 1e3, "GB/s": DUAL_BYTES / (t_dual * 1e-3) / 1e9,
+                "frac_hbm": DUAL_BYTES / (t_dual * 1e-3) / 1e9 / hbm},
             "gemm_blockscaled": {"us": t_gemm * 1e3, "TFLOP/s": gemm_tflops, "frac_fp8_peak": gemm_tflops / fp8_peak},
             "hbm_peak_gbs": hbm, "hbm_peak_source": src,
         },

@@ -40,6 +40,7 @@ _vp, _i64, _i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
 SIGNATURES = {
     "fp8_quant_act_1x128": (_i32, [_vp, _i64, _i64, _i32, _vp, _vp, _vp]),
     "fp8_quant_w_128x128": (_i32, [_vp, _i64, _i64, _vp, _vp, _vp, _vp]),
+    "fp8_quant_act_dual": (_i32, [_vp, _i64, _i64, _vp, _vp, _vp, _vp, _vp]),
     "fp8_gemm_blockscaled": (_i32, [_vp, _vp, _vp, _vp, _i32, _i64, _i64, _vp, _i32, _i64, _i64, _i64, _vp]),
     "fp8_gemm_grouped": (_i32, [_vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i64, _i64, _i64, _vp]),
     "fp8fg_status_string": (ctypes.c_char_p, [_i32]),
@@ -132,6 +133,22 @@ def fp8_quant_act_1x128(x: torch.Tensor, axis: int = FP8FG_AXIS_COLS, q=None, sc
     st = load().fp8_quant_act_1x128(_ptr(x), rows, cols, int(axis), _ptr(q), _ptr(scales), _stream(stream))
     _check(st, "fp8_quant_act_1x128")
     return q, scales
+
+
+def fp8_quant_act_dual(x: torch.Tensor, stream=None):
+    """BF16 x[rows, cols] -> (q_row, s_row, q_col_t, s_col) from one read of x:
+    the outputs of fp8_quant_act_1x128 with axis 0 and with axis 1."""
+    rows, cols = x.shape
+    if x.dtype != torch.bfloat16 or not x.is_contiguous() or not x.is_cuda:
+        raise ValueError("x must be a contiguous CUDA bfloat16 tensor")
+    q_row = torch.empty((rows, cols), dtype=torch.uint8, device=x.device)
+    s_row = torch.empty((cols // GROUP, rows), dtype=torch.float32, device=x.device)
+    q_col_t = torch.empty((cols, rows), dtype=torch.uint8, device=x.device)
+    s_col = torch.empty((rows // GROUP, cols), dtype=torch.float32, device=x.device)
+    st = load().fp8_quant_act_dual(_ptr(x), rows, cols, _ptr(q_row), _ptr(s_row), _ptr(q_col_t), _ptr(s_col),
+                                   _stream(stream))
+    _check(st, "fp8_quant_act_dual")
+    return q_row, s_row, q_col_t, s_col
 
 
 def fp8_quant_w_128x128(w: torch.Tensor, transposed: bool = False, q=None, q_t=None, scales=None, stream=None):

@@ -84,6 +84,22 @@ int fp8_quant_act_1x128(const void* x_bf16, int64_t rows, int64_t cols, int axis
     return from_cuda(launch_quant_act_cols(x_bf16, rows, cols, q, scales, d->num_sms, stream));
 }
 
+int fp8_quant_act_dual(const void* x_bf16, int64_t rows, int64_t cols, uint8_t* q_row, float* s_row,
+                       uint8_t* q_col_t, float* s_col, cudaStream_t stream) {
+    if (rows < 0 || cols < 0 || rows % 128 != 0 || cols % 128 != 0) return kErrInvalidArg;
+    if (rows == 0 || cols == 0) return kOk;
+    if (!x_bf16 || !q_row || !s_row || !q_col_t || !s_col) return kErrInvalidArg;
+    if (rows > (int64_t(1) << 40) / cols) return kErrInvalidArg;
+    // grid: (rows / 128) x (cols / 128) tiles
+    if (cols / 128 > 65535) return kErrInvalidArg;
+    if (!aligned16(x_bf16) || !aligned16(q_row) || !aligned16(s_row) || !aligned16(q_col_t) || !aligned16(s_col))
+        return kErrMisaligned;
+    DeviceInfo* d = nullptr;
+    int st = current_device(&d);
+    if (st != kOk) return st;
+    return from_cuda(launch_quant_act_dual(x_bf16, rows, cols, q_row, s_row, q_col_t, s_col, stream));
+}
+
 int fp8_quant_w_128x128(const float* w, int64_t rows, int64_t cols, uint8_t* q, uint8_t* q_t, float* scales,
                         cudaStream_t stream) {
     if (rows < 0 || cols < 0 || rows % 128 != 0 || cols % 128 != 0) return kErrInvalidArg;

@@ -12,6 +12,9 @@
 //   * 128x1 token-axis groups with a transposed (K-major) output for the
 //     weight-gradient GEMM, whose reduction runs over tokens: "DeepSeek FP8
 //     Training" (arcalunar.github.io), backward pass, Wgrad step 1.
+//   * Both of the above from one read of the BF16 tensor (the activation is
+//     cached in FP8 for the backward pass: DeepSeek-V3 FP8 post, low-precision
+//     storage paragraph): quant_act_dual_kernel.
 #include <cuda_runtime.h>
 #include <cstdint>
 
@@ -203,6 +206,107 @@ __global__ void __launch_bounds__(256) quant_act_cols_kernel(const uint4* __rest
     }
 }
 
+// ------------------------------------------------- 1 x 128 and 128 x 1 ----
+// One CTA per 128 x 128 tile of X, 256 threads.  Row pass straight from the
+// loads: half-warp h holds rows h, h+16, ..., h+112 (8 BF16 each lane), the
+// 1x128 amax by half-warp shuffles, codes to q_row.  The tile also goes to
+// shared memory (rows of 64 words + 1 pad word), where the column pass reads
+// it: thread t owns channel pair t % 64 over 32 tokens (t / 64), the 4
+// partial maxima meet in shared memory, and each thread writes 2 x 16 codes
+// per channel into q_col_t[cols, rows] (the tile is read twice, for the
+// maxima and for the codes, to keep registers low enough for 4 CTAs per SM).
+// The arithmetic is the same as the single-axis kernels', so both outputs
+// equal theirs bit for bit.
+__global__ void __launch_bounds__(256, 4) quant_act_dual_kernel(const uint4* __restrict__ x, int64_t rows, int64_t cols,
+                                                             uint2* __restrict__ q_row, float* __restrict__ s_row,
+                                                             uint8_t* __restrict__ q_col_t,
+                                                             float* __restrict__ s_col) {
+    __shared__ uint32_t tile[kGroup][kGroup / 2 + 1];
+    __shared__ float part[4][kGroup];
+    const int t = threadIdx.x, l16 = t & 15, hw = t >> 4;
+    const int64_t tb = blockIdx.x, cb = blockIdx.y;
+    const int64_t r0 = tb * kGroup, c0 = cb * kGroup;
+    uint4 v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) v[u] = __ldcs(x + ((r0 + hw + 16 * u) * cols + c0) / 8 + l16);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+        const int r = hw + 16 * u;
+        uint32_t* dst = &tile[r][4 * l16];
+        dst[0] = v[u].x;
+        dst[1] = v[u].y;
+        dst[2] = v[u].z;
+        dst[3] = v[u].w;
+        const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+        float f[8];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            f[2 * k] = bf16_lo(w[k]);
+            f[2 * k + 1] = bf16_hi(w[k]);
+        }
+        float amax = 0.0f;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) amax = fmaxf(amax, fabsf(f[k]));
+#pragma unroll
+        for (int m = 8; m >= 1; m >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, m));
+        const float s = __fdiv_rn(amax, 448.0f);
+        const GroupScale gs(s);
+        uint2 out;
+        out.x = quant_quad(f[0], f[1], f[2], f[3], gs);
+        out.y = quant_quad(f[4], f[5], f[6], f[7], gs);
+        __stcs(q_row + ((r0 + r) * cols + c0) / 8 + l16, out);
+        if (l16 == 0) s_row[cb * rows + r0 + r] = s;
+    }
+    __syncthreads();
+    const int cp = t & 63;   // channel pair: channels 2cp, 2cp+1 of the tile
+    const int rs = t >> 6;   // token segment: tokens 32rs .. 32rs+31
+    float a0 = 0.0f, a1 = 0.0f;
+#pragma unroll
+    for (int r = 0; r < 32; ++r) {
+        const uint32_t w = tile[32 * rs + r][cp];
+        a0 = fmaxf(a0, fabsf(bf16_lo(w)));
+        a1 = fmaxf(a1, fabsf(bf16_hi(w)));
+    }
+    part[rs][2 * cp] = a0;
+    part[rs][2 * cp + 1] = a1;
+    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        a0 = fmaxf(a0, part[k][2 * cp]);
+        a1 = fmaxf(a1, part[k][2 * cp + 1]);
+    }
+    const float s0 = __fdiv_rn(a0, 448.0f), s1 = __fdiv_rn(a1, 448.0f);
+    const GroupScale g0(s0), g1(s1);
+    const int64_t ch0 = c0 + 2 * cp;
+    uint4* dst0 = reinterpret_cast<uint4*>(q_col_t + ch0 * rows + r0 + 32 * rs);
+    uint4* dst1 = reinterpret_cast<uint4*>(q_col_t + (ch0 + 1) * rows + r0 + 32 * rs);
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        float lo[16], hi[16];
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+            const uint32_t w = tile[32 * rs + 16 * k + r][cp];
+            lo[r] = bf16_lo(w);
+            hi[r] = bf16_hi(w);
+        }
+        uint4 o;
+        o.x = quant_quad(lo[0], lo[1], lo[2], lo[3], g0);
+        o.y = quant_quad(lo[4], lo[5], lo[6], lo[7], g0);
+        o.z = quant_quad(lo[8], lo[9], lo[10], lo[11], g0);
+        o.w = quant_quad(lo[12], lo[13], lo[14], lo[15], g0);
+        __stcs(dst0 + k, o);
+        o.x = quant_quad(hi[0], hi[1], hi[2], hi[3], g1);
+        o.y = quant_quad(hi[4], hi[5], hi[6], hi[7], g1);
+        o.z = quant_quad(hi[8], hi[9], hi[10], hi[11], g1);
+        o.w = quant_quad(hi[12], hi[13], hi[14], hi[15], g1);
+        __stcs(dst1 + k, o);
+    }
+    if (rs == 0) {
+        s_col[tb * cols + ch0] = s0;
+        s_col[tb * cols + ch0 + 1] = s1;
+    }
+}
+
 // ---------------------------------------------------------- 128 x 128 ----
 // A CTA of 512 threads owns one 128x128 FP32 block at a time and keeps it in
 // registers: thread t holds columns 4(t%32)..+3 of rows 4(t/32)+{0..3} and
@@ -307,6 +411,14 @@ cudaError_t launch_quant_act_cols(const void* x, int64_t rows, int64_t cols, uin
     if (grid > static_cast<int64_t>(num_sms) * 8) grid = static_cast<int64_t>(num_sms) * 8;
     quant_act_cols_kernel<<<static_cast<unsigned>(grid), 256, 0, stream>>>(static_cast<const uint4*>(x), rows, cols,
                                                                            q, scales);
+    return cudaPeekAtLastError();
+}
+
+cudaError_t launch_quant_act_dual(const void* x, int64_t rows, int64_t cols, uint8_t* q_row, float* s_row,
+                                  uint8_t* q_col_t, float* s_col, cudaStream_t stream) {
+    const dim3 grid(static_cast<unsigned>(rows / kGroup), static_cast<unsigned>(cols / kGroup));
+    quant_act_dual_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint4*>(x), rows, cols,
+                                                    reinterpret_cast<uint2*>(q_row), s_row, q_col_t, s_col);
     return cudaPeekAtLastError();
 }
 

@@ -93,6 +93,27 @@ int fp8_quant_act_1x128(const void *x_bf16, int64_t rows, int64_t cols, int axis
                         uint8_t *q, float *scales, cudaStream_t stream);
 
 /*
+ * fp8_quant_act_dual -- both activation quantizations of one BF16 tensor
+ * from a single read of it: the 1x128 row groups of fp8_quant_act_1x128
+ * with axis FP8FG_AXIS_COLS and the 128x1 column groups (transposed output)
+ * of axis FP8FG_AXIS_ROWS, bit for bit the same codes and scales.  The
+ * forward pass caches the activation in FP8 for the backward pass (DeepSeek-V3
+ * FP8 post, low-precision storage paragraph), which needs the 1x128 copy for
+ * the next layer's GEMM and the token-axis copy for the weight gradient
+ * ("DeepSeek FP8 Training", Wgrad step 1).
+ *
+ *   x_bf16  [rows, cols] BF16, row-major, 16-byte aligned.
+ *   q_row   [rows, cols] E4M3 codes;       s_row [cols/128, rows] FP32.
+ *   q_col_t [cols, rows] E4M3 codes;       s_col [rows/128, cols] FP32.
+ *   rows and cols multiples of 128, cols/128 <= 65535; all buffers 16-byte
+ *   aligned and owned by the caller.  rows == 0 or cols == 0 is a no-op.
+ * Errors: FP8FG_ERR_INVALID_ARG (shape, NULL), FP8FG_ERR_MISALIGNED,
+ * FP8FG_ERR_UNSUPPORTED_DEVICE, FP8FG_ERR_CUDA (launch).
+ */
+int fp8_quant_act_dual(const void *x_bf16, int64_t rows, int64_t cols, uint8_t *q_row, float *s_row,
+                       uint8_t *q_col_t, float *s_col, cudaStream_t stream);
+
+/*
  * fp8_quant_w_128x128 -- online E4M3 quantization of an FP32 master weight
  * w[rows, cols] in 128x128 blocks ("per 128 input channels per 128 output
  * channels", Figure 7 (a) of the DeepSeek-V3 FP8 post; the FP32 master is

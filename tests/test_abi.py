@@ -22,7 +22,7 @@ def _declared_functions():
 
 def test_header_declares_the_entry_points():
     names = _declared_functions()
-    for n in ["fp8_quant_act_1x128", "fp8_quant_w_128x128", "fp8_gemm_blockscaled", "fp8_gemm_grouped",
+    for n in ["fp8_quant_act_1x128", "fp8_quant_act_dual", "fp8_quant_w_128x128", "fp8_gemm_blockscaled", "fp8_gemm_grouped",
               "fp8fg_status_string", "fp8fg_last_device_status", "fp8fg_selftest_watchdog",
               "fp8fg_set_wait_limit"]:
         assert n in names
@@ -68,6 +68,15 @@ def test_quant_act_argument_checks(lib):
     assert f(A16, 4, 128, 0, MIS, A16, None) == 2
     assert f(None, 0, 128, 0, None, None, None) == 0       # empty: no-op, nothing touched
     assert f(None, 4, 0, 0, None, None, None) == 0
+
+
+def test_quant_dual_argument_checks(lib):
+    f = lib.fp8_quant_act_dual
+    assert f(A16, 128, 100, A16, A16, A16, A16, None) == 1        # cols not a multiple of 128
+    assert f(A16, 100, 128, A16, A16, A16, A16, None) == 1        # rows not a multiple of 128
+    assert f(A16, 128, 128, A16, A16, None, A16, None) == 1       # null output
+    assert f(A16, 128, 128, A16, A16, MIS, A16, None) == 2        # misaligned
+    assert f(None, 0, 128, None, None, None, None, None) == 0     # empty: no-op
 
 
 def test_quant_w_argument_checks(lib):

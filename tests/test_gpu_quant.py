@@ -183,3 +183,42 @@ def test_weight_quotients_at_rounding_midpoints(gpu_device):
         blocks.append(blk)
     w = np.concatenate(blocks, axis=1)                      # [128, 128 * n_blocks]
     _w_parity(np.ascontiguousarray(w), gpu_device)
+
+
+def _dual_parity(xb: np.ndarray, device):
+    q_row, s_row, q_col_t, s_col = fb.fp8_quant_act_dual(dev_bf16(xb, device))
+    torch.cuda.synchronize()
+    qo, so = oracle.quant_act(xb, axis=0)
+    qto, sto = oracle.quant_act(xb, axis=1)
+    assert np.array_equal(host(s_row).view(np.uint32), so.view(np.uint32)), "row scales differ"
+    assert np.array_equal(host(q_row), qo), "row codes differ"
+    assert np.array_equal(host(s_col).view(np.uint32), sto.view(np.uint32)), "column scales differ"
+    assert np.array_equal(host(q_col_t), qto), "column codes differ"
+
+
+@pytest.mark.parametrize("shape", [(128, 128), (256, 384), (384, 1280)])
+def test_dual_small(gpu_device, shape):
+    rng = np.random.default_rng(300 + shape[1])
+    _dual_parity(synth.activations_channel_outliers(rng, *shape), gpu_device)
+
+
+def test_dual_zero_and_tiny_groups(gpu_device):
+    x = np.zeros((256, 256), np.float32)
+    x[5, 3] = -2.0
+    x[130:140, 200] = np.float32(2.0 ** -133)    # a column group and row groups with subnormal scales
+    x[200, 128:256] = -0.0
+    _dual_parity(synth.f32_to_bf16_bits(x), gpu_device)
+
+
+def test_dual_full_wgrad_x(gpu_device):
+    """X[8192,7168] of the Wgrad workload: the fused kernel against the
+    oracle on both axes, and against the two single-axis kernels."""
+    xb = synth.wgrad(seed=3)["x"]
+    _dual_parity(xb, gpu_device)
+    x = dev_bf16(xb, gpu_device)
+    q_row, s_row, q_col_t, s_col = fb.fp8_quant_act_dual(x)
+    q0, s0 = fb.fp8_quant_act_1x128(x, axis=fb.FP8FG_AXIS_COLS)
+    q1, s1 = fb.fp8_quant_act_1x128(x, axis=fb.FP8FG_AXIS_ROWS)
+    torch.cuda.synchronize()
+    assert torch.equal(q_row, q0) and torch.equal(s_row.view(torch.int32), s0.view(torch.int32))
+    assert torch.equal(q_col_t, q1) and torch.equal(s_col.view(torch.int32), s1.view(torch.int32))
