@@ -39,9 +39,9 @@ FP8FG_DEV float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 // rounded quotient.  The remainder stays exact (no underflow) whenever
 // |x / s| >= 2^-11 and s >= 2^-90; smaller quotients all encode to a signed
 // zero in E4M3 (its smallest magnitude is 2^-9, the tie to zero at 2^-10),
-// and the sign of the quotient is the sign of x (s > 0), so the result is
-// taken with x's sign.  Scales below 2^-90 fall back to the full IEEE
-// division.  Bit-exactness against the oracle's IEEE division is tested.
+// and the sign of the quotient is the sign of x (s > 0), which quant4 puts
+// into the codes.  Scales below 2^-90 fall back to the full IEEE division.
+// Bit-exactness against the oracle's IEEE division is tested.
 struct GroupScale {
     float s, r;
     int mode;  // 0: s == 0 (codes keep only the sign), 1: reciprocal correction, 2: IEEE division
@@ -55,24 +55,61 @@ struct GroupScale {
             mode = 2;
         }
     }
-    FP8FG_DEV float quot(float x) const {
-        if (mode == 2) return __fdiv_rn(x, s);
-        const float q = x * r;
-        const float rem = fmaf(-q, s, x);
-        return copysignf(fmaf(rem, r, q), x);
-    }
 };
 
-// Codes when the scale is 0: the sign of each value, nothing else.
-FP8FG_DEV uint32_t sign_pair(float a, float b) {
-    return ((__float_as_uint(a) >> 31) << 7) | ((__float_as_uint(b) >> 31) << 15);
+// Four values -> four E4M3 codes (x0 in the lowest byte).  The quotients by
+// the reciprocal correction are computed two lanes at a time (packed FP32;
+// each lane rounds exactly as the scalar operations).  The sign of each code
+// is taken from x's sign bit, ORed in at the end: a nonzero quotient already
+// carries x's sign, and a quotient that rounds to zero must encode as a signed
+// zero (0x80 for negative x), which is what the OR gives.  A zero scale leaves
+// only the signs.  `signs` holds x_k's sign bit at bit 8k+7.
+FP8FG_DEV uint32_t quant4(float x0, float x1, float x2, float x3, uint32_t signs, const GroupScale& g) {
+    if (g.mode == 0) return signs;
+    uint32_t lo, hi;
+    if (g.mode == 1) {
+        // q = RN(x r); rem = x - s q (exact, one FMA); q' = RN(q + rem r)
+        float q0 = x0, q1 = x1, q2 = x2, q3 = x3;
+        mul2(q0, q1, g.r, g.r);
+        mul2(q2, q3, g.r, g.r);
+        float e0 = x0, e1 = x1, e2 = x2, e3 = x3;
+        fma2(e0, e1, q0, q1, -g.s, -g.s);
+        fma2(e2, e3, q2, q3, -g.s, -g.s);
+        fma2(q0, q1, e0, e1, g.r, g.r);
+        fma2(q2, q3, e2, e3, g.r, g.r);
+        lo = cvt_e4m3x2(q0, q1);
+        hi = cvt_e4m3x2(q2, q3);
+    } else {
+        lo = cvt_e4m3x2(__fdiv_rn(x0, g.s), __fdiv_rn(x1, g.s));
+        hi = cvt_e4m3x2(__fdiv_rn(x2, g.s), __fdiv_rn(x3, g.s));
+    }
+    return (lo | (hi << 16)) | signs;
 }
 
-// Four values -> four E4M3 codes (a in the lowest byte).
+// Four FP32 values.
 FP8FG_DEV uint32_t quant_quad(float a, float b, float c, float d, const GroupScale& g) {
-    if (g.mode == 0) return sign_pair(a, b) | (sign_pair(c, d) << 16);
-    return static_cast<uint32_t>(cvt_e4m3x2(g.quot(a), g.quot(b))) |
-           (static_cast<uint32_t>(cvt_e4m3x2(g.quot(c), g.quot(d))) << 16);
+    const uint32_t ab = __byte_perm(__float_as_uint(a), __float_as_uint(b), 0x0073);
+    const uint32_t cd = __byte_perm(__float_as_uint(c), __float_as_uint(d), 0x0073);
+    return quant4(a, b, c, d, __byte_perm(ab, cd, 0x5410) & 0x80808080u, g);
+}
+
+// Four BF16 values in two words (value 2i in the low half of word i, 2i+1 in
+// the high half); the high byte of each BF16 value holds its sign bit.
+FP8FG_DEV uint32_t quant_quad_bf16(uint32_t w0, uint32_t w1, const GroupScale& g) {
+    return quant4(bf16_lo(w0), bf16_hi(w0), bf16_lo(w1), bf16_hi(w1), __byte_perm(w0, w1, 0x7531) & 0x80808080u, g);
+}
+
+// Max |x| of the 128 BF16 values a half-warp holds (8 per lane).  For
+// non-negative BF16 bit patterns the integer order is the numeric order, so
+// the maximum is taken on the 16-bit patterns with the sign bits cleared,
+// two at a time; the result widens to FP32 exactly.  Inputs are finite.
+FP8FG_DEV float group_amax_bf16(const uint4& v) {
+    uint32_t m = __vmaxu2(__vmaxu2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu), __vmaxu2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu));
+    // xor < 16 stays inside the half-warp that owns the group
+#pragma unroll
+    for (int k = 8; k >= 1; k >>= 1) m = __vmaxu2(m, __shfl_xor_sync(0xffffffffu, m, k));
+    const uint32_t hi = m >> 16, lo = m & 0xFFFFu;
+    return __uint_as_float((hi > lo ? hi : lo) << 16);
 }
 
 // ------------------------------------------------------------ 1 x 128 ----
@@ -99,25 +136,14 @@ __global__ void __launch_bounds__(256) quant_act_rows_kernel(const uint4* __rest
 #pragma unroll
     for (int u = 0; u < kRowU; ++u) {
         const int64_t r = r0 + 16 * u;
-        const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-        float f[8];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            f[2 * k] = bf16_lo(w[k]);
-            f[2 * k + 1] = bf16_hi(w[k]);
-        }
-        float amax = 0.0f;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) amax = fmaxf(amax, fabsf(f[k]));
         // xor < 16 stays inside the half-warp that owns the group
-#pragma unroll
-        for (int m = 8; m >= 1; m >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, m));
+        const float amax = group_amax_bf16(v[u]);
         if (r >= rows) continue;
         const float s = __fdiv_rn(amax, 448.0f);
         const GroupScale gs(s);
         uint2 out;
-        out.x = quant_quad(f[0], f[1], f[2], f[3], gs);
-        out.y = quant_quad(f[4], f[5], f[6], f[7], gs);
+        out.x = quant_quad_bf16(v[u].x, v[u].y, gs);
+        out.y = quant_quad_bf16(v[u].z, v[u].w, gs);
         __stcs(q + (r * cols + c * kGroup) / 8 + l16, out);
         if (l16 == 0) scales[c * rows + r] = s;
     }
@@ -237,23 +263,12 @@ __global__ void __launch_bounds__(256, 4) quant_act_dual_kernel(const uint4* __r
         dst[1] = v[u].y;
         dst[2] = v[u].z;
         dst[3] = v[u].w;
-        const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-        float f[8];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            f[2 * k] = bf16_lo(w[k]);
-            f[2 * k + 1] = bf16_hi(w[k]);
-        }
-        float amax = 0.0f;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) amax = fmaxf(amax, fabsf(f[k]));
-#pragma unroll
-        for (int m = 8; m >= 1; m >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, m));
+        const float amax = group_amax_bf16(v[u]);
         const float s = __fdiv_rn(amax, 448.0f);
         const GroupScale gs(s);
         uint2 out;
-        out.x = quant_quad(f[0], f[1], f[2], f[3], gs);
-        out.y = quant_quad(f[4], f[5], f[6], f[7], gs);
+        out.x = quant_quad_bf16(v[u].x, v[u].y, gs);
+        out.y = quant_quad_bf16(v[u].z, v[u].w, gs);
         __stcs(q_row + ((r0 + r) * cols + c0) / 8 + l16, out);
         if (l16 == 0) s_row[cb * rows + r0 + r] = s;
     }
