@@ -53,7 +53,9 @@ namespace fp8fg {
 namespace {
 
 constexpr int BM = 128;   // rows of A per tile (TMEM lanes)
-constexpr int BN = 256;   // rows of B per tile (TMEM columns per buffer)
+constexpr int BN = 256;   // rows of B per tile (TMEM columns per buffer): 256 or 128
+constexpr int NBUF = 512 / BN;   // TMEM accumulator buffers (all 512 columns)
+constexpr int ECOLS = BN / 2;    // columns of a tile per promotion thread
 constexpr int BK = 128;   // one quantization group along K
 constexpr int MMA_K = 32; // K per tcgen05.mma for 8-bit operands
 constexpr int EPI_WARPS = 8;
@@ -62,11 +64,11 @@ constexpr int THREADS = 128 + 32 * EPI_WARPS;
 // warpgroup 0 keeps 64 and the two promotion warpgroups take 216 each
 // (128 x 64 + 256 x 216 = 63488, within the launch total).
 constexpr int REGS_LOW = 64, REGS_HIGH = 216;
-constexpr uint32_t TMEM_COLS = 2 * BN;
+constexpr uint32_t TMEM_COLS = NBUF * BN;
 constexpr uint32_t A_BYTES = BM * BK;
 constexpr uint32_t B_BYTES = BN * BK;
-// Named barriers 1 and 2: the 8 promotion warps hand TMEM buffer b back to
-// the MMA warp through barrier 1 + b (bar.arrive by them, bar.sync by the
+// Named barriers 1 .. NBUF: the 8 promotion warps hand TMEM buffer b back
+// to the MMA warp through barrier 1 + b (bar.arrive by them, bar.sync by the
 // whole MMA warp).
 constexpr int kRelThreads = 32 * (1 + EPI_WARPS);
 // Limit of the promotion warps' wait for a chunk's commit (see run_epilogue):
@@ -78,7 +80,7 @@ constexpr uint64_t kHandoffLimitNs = 3 * kMaxWaitLimitNs;
 // the Fprop shape: the fourth leaves almost no L1 for the scale loads.)
 template <int kRowB>
 struct __align__(1024) Smem {
-    static constexpr int kStages = 3;
+    static constexpr int kStages = BN == 256 ? 3 : 4;
     static constexpr int kSlots = kRowB ? 8 : 1;
     uint8_t a[kStages][A_BYTES];
     uint8_t b[kStages][B_BYTES];
@@ -86,7 +88,7 @@ struct __align__(1024) Smem {
     float sb[kSlots][BN];
     uint64_t full[kStages];
     uint64_t empty[kStages];
-    uint64_t tfull[2];
+    uint64_t tfull[NBUF];
     uint64_t sfull[kSlots];
     uint64_t sempty[kSlots];
     uint64_t drain;
@@ -258,8 +260,8 @@ FP8FG_DEV void run_mma(Smem<kRowB>& sm, uint32_t tmem_base, const Params& p, int
     for (int64_t t = blockIdx.x; t < num_tiles; t += gridDim.x) {
         for (int64_t c = 0; c < kb; ++c, ++g) {
             const uint32_t s = g % ST, ph = (g / ST) & 1;
-            const uint32_t buf = g & 1;
-            if (g >= 2) named_sync<kRelThreads>(1 + static_cast<int>(buf));
+            const uint32_t buf = g % NBUF;
+            if (g >= NBUF) named_sync<kRelThreads>(1 + static_cast<int>(buf));
             if (ok) {
                 bool f = true;
                 if (lane == 0)
@@ -286,7 +288,7 @@ FP8FG_DEV void run_mma(Smem<kRowB>& sm, uint32_t tmem_base, const Params& p, int
         }
     }
     // the last hand-back of each buffer that was used
-    for (uint32_t b = 0; b < 2; ++b)
+    for (uint32_t b = 0; b < NBUF; ++b)
         if (g > b) named_sync<kRelThreads>(1 + static_cast<int>(b));
     if (lane == 0) {
         // every MMA issued by this thread has finished before TMEM is released
@@ -330,7 +332,7 @@ FP8FG_DEV TileScales load_tile_scales(int64_t t, const Params& p, int64_t m_tile
     TileScales ts;
     int64_t n0;
     tile_origin(t, m_tiles, n_tiles, p.m_fastest, ts.m0, n0);
-    ts.col0 = n0 + 128 * half;
+    ts.col0 = n0 + ECOLS * half;
     ts.active = ts.col0 < p.N;
     ts.sbp = p.sb;
     ts.sb_cur = 0.0f;
@@ -354,7 +356,7 @@ FP8FG_DEV void run_epilogue(Smem<kRowB>& sm, uint32_t tmem_base, const Params& p
     constexpr int SL = Smem<kRowB>::kSlots;
     volatile int* abort_flag = &sm.abort_flag;
     const int quad = warp & 3;          // TMEM lanes this warp may read: 32*quad .. 32*quad+31
-    const int half = (warp - 4) >> 2;   // columns 128*half .. 128*half+127 of the tile
+    const int half = (warp - 4) >> 2;   // columns ECOLS*half .. ECOLS*half+ECOLS-1 of the tile
     const int row = quad * 32 + lane;   // tile row owned by this thread
     const uint32_t t_lane = static_cast<uint32_t>(quad * 32) << 16;
     const uint32_t ob = smem_u32(sm.out[warp - 4]);
@@ -371,11 +373,11 @@ FP8FG_DEV void run_epilogue(Smem<kRowB>& sm, uint32_t tmem_base, const Params& p
         float sb_cur = nts.sb_cur, sb_nxt = nts.sb_nxt;
         // A scales of chunks c, c+1, c+2 in flight
         float q0 = nts.q0, q1 = nts.q1, q2 = nts.q2;
-        float acc[128];
+        float acc[ECOLS];
 #pragma unroll
-        for (int j = 0; j < 128; ++j) acc[j] = 0.0f;
+        for (int j = 0; j < ECOLS; ++j) acc[j] = 0.0f;
         for (int64_t c = 0; c < kb; ++c, ++g) {
-            const uint32_t buf = g & 1, tph = (g >> 1) & 1;
+            const uint32_t buf = g % NBUF, tph = (g / NBUF) & 1;
             const uint32_t sl = g % SL, sph = (g / SL) & 1;
             if (!kRowB && c > 0 && (c & 31) == 0) {
                 sb_cur = sb_nxt;
@@ -407,24 +409,21 @@ FP8FG_DEV void run_epilogue(Smem<kRowB>& sm, uint32_t tmem_base, const Params& p
             tc_fence_after();
             const float sbv = __shfl_sync(0xffffffffu, sb_cur, static_cast<int>(c & 31));
             if (active && !dead) {
-                const uint32_t taddr = tmem_base + t_lane + buf * BN + 128 * half;
+                const uint32_t taddr = tmem_base + t_lane + buf * BN + ECOLS * half;
                 const float scale = kRowB ? sa_i : sa_i * sbv;
-                const float* sbrow = sm.sb[sl] + 128 * half;
-                // 4 x 32 columns; the next load is in flight while the
-                // previous 32 columns are folded in
-                uint32_t ra[32], rb[32];
-                tmem_ld_32x32b_x32(taddr, ra);
-                tmem_ld_wait(ra);
-                tmem_ld_32x32b_x32(taddr + 32, rb);
-                promote32<kRowB>(acc, ra, scale, sbrow);
-                tmem_ld_wait(rb);
-                tmem_ld_32x32b_x32(taddr + 64, ra);
-                promote32<kRowB>(acc + 32, rb, scale, sbrow + 32);
-                tmem_ld_wait(ra);
-                tmem_ld_32x32b_x32(taddr + 96, rb);
-                promote32<kRowB>(acc + 64, ra, scale, sbrow + 64);
-                tmem_ld_wait(rb);
-                promote32<kRowB>(acc + 96, rb, scale, sbrow + 96);
+                const float* sbrow = sm.sb[sl] + ECOLS * half;
+                // ECOLS / 32 loads of 32 columns; the next load is in flight
+                // while the previous 32 columns are folded in
+                constexpr int NJ = ECOLS / 32;
+                uint32_t r[2][32];
+                tmem_ld_32x32b_x32(taddr, r[0]);
+                tmem_ld_wait(r[0]);
+#pragma unroll
+                for (int j = 0; j < NJ; ++j) {
+                    if (j + 1 < NJ) tmem_ld_32x32b_x32(taddr + 32 * (j + 1), r[(j + 1) & 1]);
+                    promote32<kRowB>(acc + 32 * j, r[j & 1], scale, sbrow + 32 * j);
+                    if (j + 1 < NJ) tmem_ld_wait(r[(j + 1) & 1]);
+                }
             }
             // the buffer goes back only after the loaded registers are consumed
             tc_fence_before();
@@ -441,8 +440,8 @@ FP8FG_DEV void run_epilogue(Smem<kRowB>& sm, uint32_t tmem_base, const Params& p
         // (A second staging buffer per warp was slower: above 196 KB of
         // shared memory the L1 left for the scale loads shrinks to 28 KB.)
         const int32_t gy = static_cast<int32_t>(m0 + quad * 32);
-        constexpr int kRounds = 4;   // upper bound: FP32 needs 4 rounds, BF16 2
-        const int rounds = p.out_bf16 ? 2 : 4;
+        constexpr int kRounds = ECOLS / 32;   // FP32 rounds; BF16 needs half as many
+        const int rounds = p.out_bf16 ? kRounds / 2 : kRounds;
 #pragma unroll
         for (int rd = 0; rd < kRounds; ++rd) {
             if (rd < rounds) {
@@ -452,7 +451,7 @@ FP8FG_DEV void run_epilogue(Smem<kRowB>& sm, uint32_t tmem_base, const Params& p
                 if (p.out_bf16) {
 #pragma unroll
                     for (int k = 0; k < 8; ++k) {
-                        const float* a8 = acc + 64 * (rd & 1) + 8 * k;   // rd < 2 here
+                        const float* a8 = acc + (64 * rd) % ECOLS + 8 * k;   // rd < kRounds / 2 here
                         st_shared_v4(orow + ((k ^ (lane & 7)) << 4), pack_bf16x2(a8[0], a8[1]),
                                      pack_bf16x2(a8[2], a8[3]), pack_bf16x2(a8[4], a8[5]), pack_bf16x2(a8[6], a8[7]));
                     }
@@ -492,7 +491,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             mbar_init(smem_u32(&sm.full[s]), 1);
             mbar_init(smem_u32(&sm.empty[s]), 1);
         }
-        for (int b = 0; b < 2; ++b) mbar_init(smem_u32(&sm.tfull[b]), 1);
+        for (int b = 0; b < NBUF; ++b) mbar_init(smem_u32(&sm.tfull[b]), 1);
         for (int s = 0; s < S::kSlots; ++s) {
             mbar_init(smem_u32(&sm.sfull[s]), 1);
             mbar_init(smem_u32(&sm.sempty[s]), EPI_WARPS);

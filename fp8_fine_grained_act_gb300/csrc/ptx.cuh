@@ -132,6 +132,13 @@ FP8FG_DEV void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, u
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
+// 16-byte asynchronous copy global -> shared (cache at L2 only), and the wait
+// for all of this thread's outstanding ones.
+FP8FG_DEV void cp_async_16(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src)) : "memory");
+}
+FP8FG_DEV void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 FP8FG_DEV void prefetch_tensormap(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }

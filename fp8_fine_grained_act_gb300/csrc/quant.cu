@@ -233,60 +233,57 @@ __global__ void __launch_bounds__(256) quant_act_cols_kernel(const uint4* __rest
 }
 
 // ------------------------------------------------- 1 x 128 and 128 x 1 ----
-// One CTA per 128 x 128 tile of X, 256 threads.  Row pass straight from the
-// loads: half-warp h holds rows h, h+16, ..., h+112 (8 BF16 each lane), the
-// 1x128 amax by half-warp shuffles, codes to q_row.  The tile also goes to
-// shared memory (rows of 64 words + 1 pad word), where the column pass reads
-// it: thread t owns channel pair t % 64 over 32 tokens (t / 64), the 4
-// partial maxima meet in shared memory, and each thread writes 2 x 16 codes
-// per channel into q_col_t[cols, rows] (the tile is read twice, for the
-// maxima and for the codes, to keep registers low enough for 4 CTAs per SM).
-// The arithmetic is the same as the single-axis kernels', so both outputs
-// equal theirs bit for bit.
-__global__ void __launch_bounds__(256, 4) quant_act_dual_kernel(const uint4* __restrict__ x, int64_t rows, int64_t cols,
-                                                             uint2* __restrict__ q_row, float* __restrict__ s_row,
-                                                             uint8_t* __restrict__ q_col_t,
-                                                             float* __restrict__ s_col) {
-    __shared__ uint32_t tile[kGroup][kGroup / 2 + 1];
+// One CTA per 128 x 128 tile of X, 256 threads, 5 CTAs per SM.  The tile
+// (32 KB) is copied into shared memory with cp.async (no registers held
+// while the loads are in flight), then read twice: the row pass gives
+// half-warp h rows h, h+16, ..., h+112 (8 BF16 per lane, the 1x128 amax by
+// half-warp shuffles, codes to q_row); the column pass gives thread t the
+// channel pair t % 64 over 32 tokens (t / 64), the 4 partial maxima meet in
+// shared memory, and each thread writes 2 x 16 codes per channel into
+// q_col_t[cols, rows].  A warp always reads 32 consecutive words of one row,
+// so the unpadded tile has no bank conflicts.  The arithmetic is the same as
+// the single-axis kernels', so both outputs equal theirs bit for bit.
+__global__ void __launch_bounds__(256, 5) quant_act_dual_kernel(const uint4* __restrict__ x, int64_t rows,
+                                                                int64_t cols, uint2* __restrict__ q_row,
+                                                                float* __restrict__ s_row,
+                                                                uint8_t* __restrict__ q_col_t,
+                                                                float* __restrict__ s_col) {
+    __shared__ __align__(16) uint32_t tile[kGroup][kGroup / 2];
     __shared__ float part[4][kGroup];
     const int t = threadIdx.x, l16 = t & 15, hw = t >> 4;
     const int64_t tb = blockIdx.x, cb = blockIdx.y;
     const int64_t r0 = tb * kGroup, c0 = cb * kGroup;
-    uint4 v[8];
-#pragma unroll
-    for (int u = 0; u < 8; ++u) v[u] = __ldcs(x + ((r0 + hw + 16 * u) * cols + c0) / 8 + l16);
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
         const int r = hw + 16 * u;
-        uint32_t* dst = &tile[r][4 * l16];
-        dst[0] = v[u].x;
-        dst[1] = v[u].y;
-        dst[2] = v[u].z;
-        dst[3] = v[u].w;
-        const float amax = group_amax_bf16(v[u]);
+        cp_async_16(smem_u32(&tile[r][4 * l16]), x + ((r0 + r) * cols + c0) / 8 + l16);
+    }
+    cp_async_wait_all();
+    __syncthreads();
+#pragma unroll 2
+    for (int u = 0; u < 8; ++u) {
+        const int r = hw + 16 * u;
+        const uint4 v = *reinterpret_cast<const uint4*>(&tile[r][4 * l16]);
+        const float amax = group_amax_bf16(v);
         const float s = __fdiv_rn(amax, 448.0f);
         const GroupScale gs(s);
         uint2 out;
-        out.x = quant_quad_bf16(v[u].x, v[u].y, gs);
-        out.y = quant_quad_bf16(v[u].z, v[u].w, gs);
+        out.x = quant_quad_bf16(v.x, v.y, gs);
+        out.y = quant_quad_bf16(v.z, v.w, gs);
         __stcs(q_row + ((r0 + r) * cols + c0) / 8 + l16, out);
         if (l16 == 0) s_row[cb * rows + r0 + r] = s;
     }
-    __syncthreads();
     const int cp = t & 63;   // channel pair: channels 2cp, 2cp+1 of the tile
     const int rs = t >> 6;   // token segment: tokens 32rs .. 32rs+31
-    float a0 = 0.0f, a1 = 0.0f;
+    uint32_t m2 = 0;         // both channels' maxima as 16-bit patterns
 #pragma unroll
-    for (int r = 0; r < 32; ++r) {
-        const uint32_t w = tile[32 * rs + r][cp];
-        a0 = fmaxf(a0, fabsf(bf16_lo(w)));
-        a1 = fmaxf(a1, fabsf(bf16_hi(w)));
-    }
-    part[rs][2 * cp] = a0;
-    part[rs][2 * cp + 1] = a1;
+    for (int r = 0; r < 32; ++r) m2 = __vmaxu2(m2, tile[32 * rs + r][cp] & 0x7FFF7FFFu);
+    part[rs][2 * cp] = __uint_as_float(m2 << 16);
+    part[rs][2 * cp + 1] = __uint_as_float(m2 & 0xFFFF0000u);
     __syncthreads();
+    float a0 = part[0][2 * cp], a1 = part[0][2 * cp + 1];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
+    for (int k = 1; k < 4; ++k) {
         a0 = fmaxf(a0, part[k][2 * cp]);
         a1 = fmaxf(a1, part[k][2 * cp + 1]);
     }
@@ -297,23 +294,20 @@ __global__ void __launch_bounds__(256, 4) quant_act_dual_kernel(const uint4* __r
     uint4* dst1 = reinterpret_cast<uint4*>(q_col_t + (ch0 + 1) * rows + r0 + 32 * rs);
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
-        float lo[16], hi[16];
+        uint32_t w[16];
 #pragma unroll
-        for (int r = 0; r < 16; ++r) {
-            const uint32_t w = tile[32 * rs + 16 * k + r][cp];
-            lo[r] = bf16_lo(w);
-            hi[r] = bf16_hi(w);
-        }
+        for (int r = 0; r < 16; ++r) w[r] = tile[32 * rs + 16 * k + r][cp];
         uint4 o;
-        o.x = quant_quad(lo[0], lo[1], lo[2], lo[3], g0);
-        o.y = quant_quad(lo[4], lo[5], lo[6], lo[7], g0);
-        o.z = quant_quad(lo[8], lo[9], lo[10], lo[11], g0);
-        o.w = quant_quad(lo[12], lo[13], lo[14], lo[15], g0);
+        // channel 2cp: the low halves of four consecutive tokens' words
+        o.x = quant_quad(bf16_lo(w[0]), bf16_lo(w[1]), bf16_lo(w[2]), bf16_lo(w[3]), g0);
+        o.y = quant_quad(bf16_lo(w[4]), bf16_lo(w[5]), bf16_lo(w[6]), bf16_lo(w[7]), g0);
+        o.z = quant_quad(bf16_lo(w[8]), bf16_lo(w[9]), bf16_lo(w[10]), bf16_lo(w[11]), g0);
+        o.w = quant_quad(bf16_lo(w[12]), bf16_lo(w[13]), bf16_lo(w[14]), bf16_lo(w[15]), g0);
         __stcs(dst0 + k, o);
-        o.x = quant_quad(hi[0], hi[1], hi[2], hi[3], g1);
-        o.y = quant_quad(hi[4], hi[5], hi[6], hi[7], g1);
-        o.z = quant_quad(hi[8], hi[9], hi[10], hi[11], g1);
-        o.w = quant_quad(hi[12], hi[13], hi[14], hi[15], g1);
+        o.x = quant_quad(bf16_hi(w[0]), bf16_hi(w[1]), bf16_hi(w[2]), bf16_hi(w[3]), g1);
+        o.y = quant_quad(bf16_hi(w[4]), bf16_hi(w[5]), bf16_hi(w[6]), bf16_hi(w[7]), g1);
+        o.z = quant_quad(bf16_hi(w[8]), bf16_hi(w[9]), bf16_hi(w[10]), bf16_hi(w[11]), g1);
+        o.w = quant_quad(bf16_hi(w[12]), bf16_hi(w[13]), bf16_hi(w[14]), bf16_hi(w[15]), g1);
         __stcs(dst1 + k, o);
     }
     if (rs == 0) {
