@@ -15,8 +15,13 @@ clocks seen during the timed region, and the CPU oracle timed on a bounded
 sample of the same workload.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload fprop|dgrad|wgrad|grouped]
 
 For N > 1 launch with torchrun (one rank per GPU); rank 0 prints the line.
+--workload other than fprop times the same kernels on the other GEMMs of
+the FP8 path (Dgrad dY[8192,2048] x W[2048,7168]; Wgrad dY^T X with
+X[8192,7168], token-axis groups; grouped MoE 64 experts W_g[2048,7168] over
+32768 tokens) on one GPU and prints a line of the same metric for it.
 """
 from __future__ import annotations
 
@@ -376,6 +381,137 @@ def run_gpu(args):
         dist.destroy_process_group()
 
 
+def run_other(args):
+    """One step of another GEMM of the path (quantizers + GEMM), single GPU,
+    CUDA events per kernel; the line has the same metric and a per-kernel
+    breakdown."""
+    import torch
+
+    from fp8_fine_grained_act_gb300 import binding as fb
+    from fp8_fine_grained_act_gb300 import build as fbuild
+    from fp8_fine_grained_act_gb300 import synth
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py: no CUDA device; the FP8 path has no CPU fallback")
+    fbuild.build()
+    fb.load()
+    dev = torch.device("cuda", 0)
+    bf = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+    kernels = []   # (name, fn, algorithmic bytes or None)
+    if args.workload == "dgrad":
+        d = synth.dgrad(seed=2)
+        dy, w = bf(d["dy"]), torch.from_numpy(d["w"]).to(dev)
+        Mw, Kw = dy.shape
+        Nw = w.shape[1]
+        qdy = torch.empty((Mw, Kw), dtype=torch.uint8, device=dev)
+        sdy = torch.empty((Kw // 128, Mw), dtype=torch.float32, device=dev)
+        out = {}
+
+        def k_act():
+            fb.fp8_quant_act_1x128(dy, q=qdy, scales=sdy)
+
+        def k_w():
+            out["w"] = fb.fp8_quant_w_128x128(w, transposed=True)
+
+        k_w()
+        y = torch.empty((Mw, Nw), dtype=torch.bfloat16, device=dev)
+
+        def k_gemm():
+            fb.fp8_gemm_blockscaled(qdy, sdy, out["w"][1], out["w"][2], sb_strides=(1, Nw // 128), d=y)
+
+        kernels = [("quant_act_1x128 dY", k_act, Mw * Kw * 3.031),
+                   ("quant_w_128x128 W + transposed copy", k_w, Kw * Nw * 6.0002), ("gemm_blockscaled", k_gemm, None)]
+        workload = "Dgrad: dX[8192,7168] = dY[8192,2048] . W[2048,7168], block scales read transposed, bf16 out; seed 2"
+    elif args.workload == "wgrad":
+        d = synth.wgrad(seed=3)
+        dy, x = bf(d["dy"]), bf(d["x"])
+        T, Mw = dy.shape
+        Nw = x.shape[1]
+        Kw = T
+        res = {}
+
+        def k_dy():
+            res["a"] = fb.fp8_quant_act_1x128(dy, axis=fb.FP8FG_AXIS_ROWS)
+
+        def k_x():
+            res["b"] = fb.fp8_quant_act_1x128(x, axis=fb.FP8FG_AXIS_ROWS)
+
+        k_dy()
+        k_x()
+        y = torch.empty((Mw, Nw), dtype=torch.float32, device=dev)
+
+        def k_gemm():
+            fb.fp8_gemm_blockscaled(res["a"][0], res["a"][1], res["b"][0], res["b"][1], bscale=fb.FP8FG_BSCALE_ROW,
+                                    out_dtype=fb.FP8FG_OUT_F32, d=y)
+
+        kernels = [("quant_act_128x1 dY", k_dy, T * Mw * 3.031), ("quant_act_128x1 X", k_x, T * Nw * 3.031),
+                   ("gemm_blockscaled (per-row B scales)", k_gemm, None)]
+        workload = "Wgrad: dW[2048,7168] = dY^T . X over 8192 tokens, 128x1 groups, per-row B scales, fp32 out; seed 3"
+    else:
+        d = synth.grouped_moe(seed=4)
+        x = bf(d["x"])
+        G, Nw, Kw = d["w"].shape
+        w = torch.from_numpy(d["w"].reshape(G * Nw, Kw)).to(dev)
+        off = torch.from_numpy(d["offsets"]).to(dev)
+        Mw = x.shape[0]
+        del d
+        res = {}
+
+        def k_act():
+            res["a"] = fb.fp8_quant_act_1x128(x)
+
+        def k_w():
+            res["b"] = fb.fp8_quant_w_128x128(w, transposed=False)
+
+        k_act()
+        k_w()
+        y = torch.empty((Mw, Nw), dtype=torch.bfloat16, device=dev)
+
+        def k_gemm():
+            fb.fp8_gemm_grouped(res["a"][0], res["a"][1], res["b"][0].view(G, Nw, Kw),
+                                res["b"][1].view(G, Nw // 128, Kw // 128), off, d=y)
+
+        kernels = [("quant_act_1x128 X_all", k_act, Mw * Kw * 3.031),
+                   ("quant_w_128x128 64 experts", k_w, G * Nw * Kw * 5.0002), ("gemm_grouped", k_gemm, None)]
+        workload = (f"Grouped MoE Fprop: 64 experts W_g[2048,7168], Dirichlet(1)/multinomial counts over 32768 "
+                    f"tokens padded to 128 (M_total {Mw}); bf16 out; seed 4")
+    flops = 2.0 * Mw * Nw * Kw
+    for _ in range(args.warmup):
+        for _, fn, _ in kernels:
+            fn()
+    torch.cuda.synchronize()
+    assert fb.fp8fg_last_device_status() == 0
+    steps = min(args.steps, 200)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(kernels) + 1)] for _ in range(steps)]
+    with ClockSampler(0) as clk:
+        for i in range(steps):
+            ev[i][0].record()
+            for j, (_, fn, _) in enumerate(kernels):
+                fn()
+                ev[i][j + 1].record()
+        torch.cuda.synchronize()
+    if fb.fp8fg_last_device_status() != 0:
+        raise SystemExit("device status not clean")
+    hbm, bf16, src = peaks()
+    fp8_peak = bf16 * FP8_OVER_BF16
+    per = [sum(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(steps)) / steps for j in range(len(kernels))]
+    ms = sum(per)
+    kd = {}
+    for (name, _, nbytes), t in zip(kernels, per):
+        if nbytes is None:
+            tf = flops / (t * 1e-3) / 1e12
+            kd[name] = {"us": t * 1e3, "TFLOP/s": tf, "frac_fp8_peak": tf / fp8_peak}
+        else:
+            kd[name] = {"us": t * 1e3, "GB/s": nbytes / (t * 1e-3) / 1e9, "frac_hbm": nbytes / (t * 1e-3) / 1e9 / hbm}
+    line = {"metric": METRIC, "value": flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "n_gpus": 1, "steps": steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "e4m3", "data": "synthetic",
+            "config": {"workload": workload, "M": Mw, "N": Nw, "K": Kw, "parallelism": "single GPU"},
+            "kernels": kd, "peaks": {"fp8_tflops": fp8_peak, "hbm_gbs": hbm, "source": src},
+            "clocks": clk.summary(), "gpu_launches": len(kernels) * steps}
+    print(json.dumps(line), flush=True)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -383,6 +519,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", choices=["fprop", "dgrad", "wgrad", "grouped"], default="fprop")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -390,6 +527,9 @@ def main(argv=None):
         rank, _, _ = dist_env()
         if rank == 0:
             run_reference(args)
+        return
+    if args.workload != "fprop":
+        run_other(args)
         return
     run_gpu(args)
 
