@@ -242,7 +242,11 @@ __global__ void __launch_bounds__(256) quant_act_cols_kernel(const uint4* __rest
 // shared memory, and each thread writes 2 x 16 codes per channel into
 // q_col_t[cols, rows].  A warp always reads 32 consecutive words of one row,
 // so the unpadded tile has no bank conflicts.  The arithmetic is the same as
-// the single-axis kernels', so both outputs equal theirs bit for bit.
+// the single-axis kernels', so both outputs equal theirs bit for bit.  With
+// kRowPass = false it is the 128x1 quantizer alone, used when cols is a
+// multiple of 128 (a staged 1x128-only version measured no faster than
+// quant_act_rows_kernel).
+template <bool kRowPass>
 __global__ void __launch_bounds__(256, 5) quant_act_dual_kernel(const uint4* __restrict__ x, int64_t rows,
                                                                 int64_t cols, uint2* __restrict__ q_row,
                                                                 float* __restrict__ s_row,
@@ -261,7 +265,7 @@ __global__ void __launch_bounds__(256, 5) quant_act_dual_kernel(const uint4* __r
     cp_async_wait_all();
     __syncthreads();
 #pragma unroll 2
-    for (int u = 0; u < 8; ++u) {
+    for (int u = 0; u < (kRowPass ? 8 : 0); ++u) {
         const int r = hw + 16 * u;
         const uint4 v = *reinterpret_cast<const uint4*>(&tile[r][4 * l16]);
         const float amax = group_amax_bf16(v);
@@ -415,6 +419,12 @@ cudaError_t launch_quant_act_rows(const void* x, int64_t rows, int64_t cols, uin
 
 cudaError_t launch_quant_act_cols(const void* x, int64_t rows, int64_t cols, uint8_t* q, float* scales, int num_sms,
                                   cudaStream_t stream) {
+    if (cols % kGroup == 0 && cols / kGroup <= 65535) {
+        const dim3 grid(static_cast<unsigned>(rows / kGroup), static_cast<unsigned>(cols / kGroup));
+        quant_act_dual_kernel<false><<<grid, 256, 0, stream>>>(static_cast<const uint4*>(x), rows, cols, nullptr,
+                                                               nullptr, q, scales);
+        return cudaPeekAtLastError();
+    }
     const int64_t tiles = (rows / kGroup) * ((cols + kColTileC - 1) / kColTileC);
     int64_t grid = tiles;
     if (grid > static_cast<int64_t>(num_sms) * 8) grid = static_cast<int64_t>(num_sms) * 8;
@@ -426,8 +436,8 @@ cudaError_t launch_quant_act_cols(const void* x, int64_t rows, int64_t cols, uin
 cudaError_t launch_quant_act_dual(const void* x, int64_t rows, int64_t cols, uint8_t* q_row, float* s_row,
                                   uint8_t* q_col_t, float* s_col, cudaStream_t stream) {
     const dim3 grid(static_cast<unsigned>(rows / kGroup), static_cast<unsigned>(cols / kGroup));
-    quant_act_dual_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint4*>(x), rows, cols,
-                                                    reinterpret_cast<uint2*>(q_row), s_row, q_col_t, s_col);
+    quant_act_dual_kernel<true><<<grid, 256, 0, stream>>>(static_cast<const uint4*>(x), rows, cols,
+                                                          reinterpret_cast<uint2*>(q_row), s_row, q_col_t, s_col);
     return cudaPeekAtLastError();
 }
 
