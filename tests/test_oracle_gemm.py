@@ -202,16 +202,20 @@ def test_tolerance_helpers():
 
 
 def test_synthetic_workload_recipes():
-    d = synth.grouped_moe(seed=4, with_weights=False)
-    off = d["offsets"]
+    # the grouped workload's group sizes (the same first draws as grouped_moe(seed=4))
+    counts, padded, off = synth.moe_group_sizes(np.random.default_rng(4))
     assert off.dtype == np.int32 and off.shape == (65,)
     assert np.all(off % 128 == 0) and np.all(np.diff(off) >= 0)
-    assert int(d["counts"].sum()) == 32768
-    assert d["x"].shape == (int(off[-1]), 7168)
-    # pad rows are zero
-    g = int(np.argmax(d["padded"] - d["counts"]))
-    r = int(off[g] + d["counts"][g])
+    assert int(counts.sum()) == 32768
+    assert int(off[-1]) == 37120                   # M_total of the seed-4 draw
+    # the token rows: N(0,1) then zero pad rows, per expert (the full recipe on 16 channels)
+    d = synth.grouped_moe(seed=4, K=16, with_weights=False)
+    assert np.array_equal(d["offsets"], off)
+    assert d["x"].shape == (int(off[-1]), 16)
+    g = int(np.argmax(padded - counts))
+    r = int(off[g] + counts[g])
     assert np.all(d["x"][r:int(off[g + 1])] == 0)
+    assert np.all(d["x"][int(off[g]):r] != 0)
     t = synth.tiny_fprop(seed=0)
     x = synth.bf16_bits_to_f32(t["x"])
     assert x.shape == (256, 512) and t["w"].shape == (256, 512)
