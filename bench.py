@@ -93,10 +93,15 @@ def peaks():
 
 
 def gemm_source_sha() -> str:
+    """Hash of the GEMM's code (gemm.cu + ptx.cuh) with // comments and blank
+    lines left out, so that a comment edit does not orphan a profile."""
     h = hashlib.sha256()
     for rel in ("fp8_fine_grained_act_gb300/csrc/gemm.cu", "fp8_fine_grained_act_gb300/csrc/ptx.cuh"):
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
+            for line in f:
+                code = re.sub(r"//.*$", "", line).rstrip()
+                if code:
+                    h.update(code.encode() + b"\n")
     return h.hexdigest()[:16]
 
 

@@ -19,9 +19,8 @@
 // warpgroup 0 gives registers to the promotion warpgroups with setmaxnreg):
 //   warp 0      TMA producer: A tile [128 x 128 B] and B tile [256 x 128 B]
 //               per K chunk into a 3-stage shared-memory ring (128-byte
-//               swizzle), plus,
-//               for per-row B scales, the chunk's 256 B scales into a ring
-//               of their own; everything completes on mbarriers;
+//               swizzle) and, for per-row B scales, the chunk's B scales
+//               into a ring of their own; everything completes on mbarriers;
 //   warp 1      MMA issuer (lane 0 issues, the warp waits): before reusing a
 //               TMEM buffer it takes the buffer back from the promotion
 //               warps on a named barrier (bar.sync), then 4 x
@@ -31,12 +30,13 @@
 //   warps 2-3   idle;
 //   warps 4-11  promotion: wait for the buffer, tcgen05.ld 4 x 32 columns
 //               (the next load in flight while the previous 32 columns are
-//               scaled and added with packed FP32 FMAs), hand the buffer
-//               back (bar.arrive), and after the tile's last chunk write the 128 x 256
-//               outputs through shared memory with TMA stores.  The A scales
-//               come straight from global memory, three chunks ahead, into
-//               registers; block B scales come 32 chunks per load, one per
-//               lane, and are broadcast by shuffles.
+//               scaled and added with packed FP32 FMAs), hand the buffer back
+//               (bar.arrive), and after the tile's last chunk write the
+//               128 x 256 outputs through shared memory with TMA stores.  The
+//               A scales come straight from global memory, three chunks
+//               ahead, into registers (a tile's first ones during the previous
+//               tile's stores); block B scales come 32 chunks per load, one
+//               per lane, and are broadcast by shuffles.
 // The MMA of chunk c+1 runs while the promotion warps fold chunk c.
 #include <cuda.h>
 #include <cuda_runtime.h>
