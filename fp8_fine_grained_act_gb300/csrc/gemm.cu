@@ -28,8 +28,8 @@
 //               two 256-column buffers, and commits to the stage's "empty"
 //               mbarrier and the buffer's "full" one;
 //   warps 2-3   idle;
-//   warps 4-11  promotion: wait for the buffer, tcgen05.ld 4 x 32 columns
-//               (the next load in flight while the previous 32 columns are
+//   warps 4-11  promotion: wait for the buffer, tcgen05.ld 8 x 16 columns
+//               (the next load in flight while the previous 16 columns are
 //               scaled and added with packed FP32 FMAs), hand the buffer back
 //               (bar.arrive), and after the tile's last chunk write the
 //               128 x 256 outputs through shared memory with TMA stores.  The
@@ -299,12 +299,12 @@ FP8FG_DEV void run_mma(Smem<kRowB>& sm, uint32_t tmem_base, const Params& p, int
 }
 
 // ------------------------------------------------------------ promotion ---
-// acc[0..31] += P[0..31] * scale (block B scales) or
-// acc[0..31] += (P[0..31] * sbrow[0..31]) * sa (per-row B scales).
+// acc[0..15] += P[0..15] * scale (block B scales) or
+// acc[0..15] += (P[0..15] * sbrow[0..15]) * sa (per-row B scales).
 template <int kRowB>
-FP8FG_DEV void promote32(float* acc, const uint32_t (&r)[32], float scale, const float* sbrow) {
+FP8FG_DEV void promote16(float* acc, const uint32_t (&r)[16], float scale, const float* sbrow) {
 #pragma unroll
-    for (int k = 0; k < 32; k += 2) {
+    for (int k = 0; k < 16; k += 2) {
         float x0 = __uint_as_float(r[k]), x1 = __uint_as_float(r[k + 1]);
         if (kRowB) {
             const float2 s2 = *reinterpret_cast<const float2*>(sbrow + k);
@@ -412,16 +412,17 @@ FP8FG_DEV void run_epilogue(Smem<kRowB>& sm, uint32_t tmem_base, const Params& p
                 const uint32_t taddr = tmem_base + t_lane + buf * BN + ECOLS * half;
                 const float scale = kRowB ? sa_i : sa_i * sbv;
                 const float* sbrow = sm.sb[sl] + ECOLS * half;
-                // ECOLS / 32 loads of 32 columns; the next load is in flight
-                // while the previous 32 columns are folded in
-                constexpr int NJ = ECOLS / 32;
-                uint32_t r[2][32];
-                tmem_ld_32x32b_x32(taddr, r[0]);
+                // ECOLS / 16 loads of 16 columns; the next load is in flight
+                // while the previous 16 columns are folded in (16, not 32:
+                // with 32 the registers spilled)
+                constexpr int NJ = ECOLS / 16;
+                uint32_t r[2][16];
+                tmem_ld_32x32b_x16(taddr, r[0]);
                 tmem_ld_wait(r[0]);
 #pragma unroll
                 for (int j = 0; j < NJ; ++j) {
-                    if (j + 1 < NJ) tmem_ld_32x32b_x32(taddr + 32 * (j + 1), r[(j + 1) & 1]);
-                    promote32<kRowB>(acc + 32 * j, r[j & 1], scale, sbrow + 32 * j);
+                    if (j + 1 < NJ) tmem_ld_32x32b_x16(taddr + 16 * (j + 1), r[(j + 1) & 1]);
+                    promote16<kRowB>(acc + 16 * j, r[j & 1], scale, sbrow + 16 * j);
                     if (j + 1 < NJ) tmem_ld_wait(r[(j + 1) & 1]);
                 }
             }

@@ -190,14 +190,25 @@ FP8FG_DEV void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32]) {
         : "r"(taddr));
 }
 
+// 32 lanes x 16 consecutive FP32 columns.
+FP8FG_DEV void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+
 FP8FG_DEV void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // tcgen05.wait::ld that also marks the loaded registers as written there, so
 // no use of them can be scheduled before the wait.
-FP8FG_DEV void tmem_ld_wait(uint32_t (&r)[32]) {
+template <int L>
+FP8FG_DEV void tmem_ld_wait(uint32_t (&r)[L]) {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
-    for (int k = 0; k < 32; ++k) asm volatile("" : "+r"(r[k]));
+    for (int k = 0; k < L; ++k) asm volatile("" : "+r"(r[k]));
 }
 
 // --------------------------------------------------- packed FP32 (x2) ---
