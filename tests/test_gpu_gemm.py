@@ -230,3 +230,22 @@ def test_wgrad_full_sampled(gpu_device):
     ii, jj = _entries(rng, len(ci), len(cj))
     o, m = oracle.gemm_entries(qa, sa, qb, sb, ii, jj, bscale=oracle.BSCALE_ROW)
     assert_gemm_close(dwh[ci[ii], cj[jj]], o, m, "f32", "wgrad full")
+
+
+def test_calls_on_a_side_stream(gpu_device):
+    """Every entry point honours its stream argument: the Fprop chain issued
+    on a non-default stream gives the default stream's results bit for bit."""
+    d = synth.fprop_linear(seed=1, M=256, N=512, K=1024)
+    x, w = dev_bf16(d["x"], gpu_device), dev(d["w"], gpu_device)
+    qx0, sx0 = fb.fp8_quant_act_1x128(x)
+    qw0, sw0 = fb.fp8_quant_w_128x128(w, transposed=False)
+    y0 = fb.fp8_gemm_blockscaled(qx0, sx0, qw0, sw0, out_dtype=F32)
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    with torch.cuda.stream(side):
+        qx1, sx1 = fb.fp8_quant_act_1x128(x, stream=side)
+        qw1, sw1 = fb.fp8_quant_w_128x128(w, transposed=False, stream=side)
+        y1 = fb.fp8_gemm_blockscaled(qx1, sx1, qw1, sw1, out_dtype=F32, stream=side)
+    side.synchronize()
+    assert torch.equal(qx0, qx1) and torch.equal(qw0, qw1)
+    assert torch.equal(y0, y1)

@@ -28,10 +28,14 @@ def _quant_experts_gpu(w_g, device):
     return qb, sb
 
 
-@pytest.mark.parametrize("out_dtype", [fb.FP8FG_OUT_BF16, fb.FP8FG_OUT_F32])
-def test_grouped_small(gpu_device, out_dtype):
+@pytest.mark.parametrize("out_dtype,counts", [
+    (fb.FP8FG_OUT_BF16, [100, 0, 300, 128, 5]),
+    (fb.FP8FG_OUT_F32, [100, 0, 300, 128, 5]),
+    (fb.FP8FG_OUT_BF16, [0, 0, 256, 1, 0]),          # empty experts first and last
+])
+def test_grouped_small(gpu_device, out_dtype, counts):
     rng = np.random.default_rng(21)
-    counts = np.array([100, 0, 300, 128, 5])
+    counts = np.array(counts)
     padded = ((counts + 127) // 128) * 128
     offsets = np.zeros(len(counts) + 1, np.int32)
     offsets[1:] = np.cumsum(padded)
