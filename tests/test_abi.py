@@ -132,3 +132,20 @@ def test_no_device_means_an_error_not_a_fallback(lib):
     # valid arguments reach the device probe, which fails: no CPU path exists
     st = lib.fp8_quant_act_1x128(A16, 4, 128, 0, A16, A16, None)
     assert st in (3, 4)
+
+
+def test_binding_rejects_host_tensors_before_any_call(lib):
+    """The Python binding only marshals: tensors that are not contiguous CUDA
+    tensors of the right dtype are refused with ValueError, before the C ABI
+    (and any device) is reached."""
+    import torch
+    from fp8_fine_grained_act_gb300 import binding as b
+    x = torch.zeros((128, 128), dtype=torch.bfloat16)                # host tensor
+    with pytest.raises(ValueError):
+        b.fp8_quant_act_1x128(x)
+    with pytest.raises(ValueError):
+        b.fp8_quant_act_dual(x)
+    with pytest.raises(ValueError):
+        b.fp8_quant_act_1x128(torch.zeros((128, 128), dtype=torch.float32))
+    with pytest.raises(ValueError):
+        b._need(torch.zeros((4, 4)), torch.float32, (4, 4), "d")    # right dtype and shape, not on a GPU
