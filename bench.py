@@ -15,13 +15,14 @@ clocks seen during the timed region, and the CPU oracle timed on a bounded
 sample of the same workload.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload fprop|dgrad|wgrad|grouped]
+                  [--workload fprop|tiny|dgrad|wgrad|grouped]
 
 For N > 1 launch with torchrun (one rank per GPU); rank 0 prints the line.
 --workload other than fprop times the same kernels on the other GEMMs of
-the FP8 path (Dgrad dY[8192,2048] x W[2048,7168]; Wgrad dY^T X with
-X[8192,7168], token-axis groups; grouped MoE 64 experts W_g[2048,7168] over
-32768 tokens) on one GPU and prints a line of the same metric for it.
+the FP8 path (the tiny 256x256x512 Fprop; Dgrad dY[8192,2048] x
+W[2048,7168]; Wgrad dY^T X with X[8192,7168], token-axis groups; grouped MoE
+64 experts W_g[2048,7168] over 32768 tokens) on one GPU and prints a line of
+the same metric for it.
 """
 from __future__ import annotations
 
@@ -447,7 +448,44 @@ def run_other(args):
     dev = torch.device("cuda", 0)
     bf = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
     kernels = []   # (name, fn, algorithmic bytes or None)
-    if args.workload == "dgrad":
+    extra = {}
+    if args.workload == "tiny":
+        d = synth.tiny_fprop(seed=0)
+        x, w = bf(d["x"]), torch.from_numpy(d["w"]).to(dev)
+        Mw, Kw = x.shape
+        Nw = w.shape[0]
+        qx = torch.empty((Mw, Kw), dtype=torch.uint8, device=dev)
+        sx = torch.empty((Kw // 128, Mw), dtype=torch.float32, device=dev)
+        qw = torch.empty((Nw, Kw), dtype=torch.uint8, device=dev)
+        sw = torch.empty((Nw // 128, Kw // 128), dtype=torch.float32, device=dev)
+        y = torch.empty((Mw, Nw), dtype=torch.float32, device=dev)
+
+        def k_act():
+            fb.fp8_quant_act_1x128(x, q=qx, scales=sx)
+
+        def k_w():
+            fb.fp8_quant_w_128x128(w, q=qw, scales=sw)
+
+        def k_gemm():
+            fb.fp8_gemm_blockscaled(qx, sx, qw, sw, out_dtype=fb.FP8FG_OUT_F32, d=y)
+
+        # the same three calls captured once in a CUDA graph and replayed:
+        # this shape is bound by launch overhead, which the graph removes
+        for fn in (k_act, k_w, k_gemm):
+            fn()
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            k_act()
+            k_w()
+            k_gemm()
+        extra["graph"] = graph
+
+        kernels = [("quant_act_1x128 X", k_act, Mw * Kw * 3.031), ("quant_w_128x128 W", k_w, Nw * Kw * 5.0002),
+                   ("gemm_blockscaled", k_gemm, None)]
+        workload = ("Tiny Fprop: X[256,512] N(0,1) with 0.1% of entries x100, W[256,512] N(0,0.02^2), fp32 out; "
+                    "seed 0 (launch-latency bound: two 128x256 tiles)")
+    elif args.workload == "dgrad":
         d = synth.dgrad(seed=2)
         dy, w = bf(d["dy"]), torch.from_numpy(d["w"]).to(dev)
         Mw, Kw = dy.shape
@@ -552,6 +590,19 @@ def run_other(args):
             kd[name] = {"us": t * 1e3, "TFLOP/s": tf, "frac_fp8_peak": tf / fp8_peak}
         else:
             kd[name] = {"us": t * 1e3, "GB/s": nbytes / (t * 1e-3) / 1e9, "frac_hbm": nbytes / (t * 1e-3) / 1e9 / hbm}
+    if "graph" in extra:
+        g = extra["graph"]
+        for _ in range(10):
+            g.replay()
+        torch.cuda.synchronize()
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        g0.record()
+        for _ in range(steps):
+            g.replay()
+        g1.record()
+        torch.cuda.synchronize()
+        graph_ms = g0.elapsed_time(g1) / steps
+        kd["step as one CUDA graph (3 kernels)"] = {"us": graph_ms * 1e3, "TFLOP/s": flops / (graph_ms * 1e-3) / 1e12}
     line = {"metric": METRIC, "value": flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "n_gpus": 1, "steps": steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "e4m3", "data": "synthetic",
@@ -568,7 +619,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", choices=["fprop", "dgrad", "wgrad", "grouped"], default="fprop")
+    ap.add_argument("--workload", choices=["fprop", "tiny", "dgrad", "wgrad", "grouped"], default="fprop")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
