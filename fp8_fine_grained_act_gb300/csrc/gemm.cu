@@ -174,6 +174,7 @@ FP8FG_DEV int expert_of(const int32_t* offsets, int G, int64_t m0) {
 
 // Wait that ignores the abort flag (tear-down): bounded by `limit_ns`.
 FP8FG_DEV bool wait_plain(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+    if (mbar_try_wait(bar, parity)) return true;   // no timer read on the fast path
     const uint64_t t0 = globaltimer_ns();
     while (!mbar_try_wait(bar, parity))
         if (globaltimer_ns() - t0 > limit_ns) return false;
