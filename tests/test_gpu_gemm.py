@@ -249,3 +249,39 @@ def test_calls_on_a_side_stream(gpu_device):
     side.synchronize()
     assert torch.equal(qx0, qx1) and torch.equal(qw0, qw1)
     assert torch.equal(y0, y1)
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_random_shapes_against_the_oracle(gpu_device, seed):
+    """Random shapes (multiples of 128, ragged against the 128x256 tile),
+    block or per-row B scales, BF16 or FP32 output: the whole output against
+    the oracle, on operands quantized by the GPU and checked byte for byte."""
+    rng = np.random.default_rng(1000 + seed)
+    M, N, K = (int(rng.integers(1, 5)) * 128, int(rng.integers(1, 7)) * 128, int(rng.integers(1, 9)) * 128)
+    row_b = bool(seed % 3 == 2)
+    out_dtype = F32 if seed % 2 else BF16
+    if row_b:
+        # Wgrad-like: both operands from token-axis groups (K = tokens)
+        a_src = synth.gradients_token_outliers(rng, K, M)
+        b_src = synth.activations_channel_outliers(rng, K, N)
+        qa, sa = fb.fp8_quant_act_1x128(dev_bf16(a_src, gpu_device), axis=fb.FP8FG_AXIS_ROWS)
+        qb, sb = fb.fp8_quant_act_1x128(dev_bf16(b_src, gpu_device), axis=fb.FP8FG_AXIS_ROWS)
+        d = fb.fp8_gemm_blockscaled(qa, sa, qb, sb, bscale=fb.FP8FG_BSCALE_ROW, out_dtype=out_dtype)
+        qa_o, sa_o = oracle.quant_act(a_src, axis=1)
+        qb_o, sb_o = oracle.quant_act(b_src, axis=1)
+        bscale = oracle.BSCALE_ROW
+    else:
+        a_src = synth.activations_random_outliers(rng, M, K)
+        b_src = synth.master_weight(rng, N, K)
+        qa, sa = fb.fp8_quant_act_1x128(dev_bf16(a_src, gpu_device))
+        qb, sb = fb.fp8_quant_w_128x128(dev(b_src, gpu_device))
+        d = fb.fp8_gemm_blockscaled(qa, sa, qb, sb, out_dtype=out_dtype)
+        qa_o, sa_o = oracle.quant_act(a_src)
+        qb_o, sb_o = oracle.quant_w(b_src)
+        bscale = oracle.BSCALE_BLOCK128
+    torch.cuda.synchronize()
+    assert np.array_equal(host(qa), qa_o) and np.array_equal(host(qb), qb_o)
+    assert np.array_equal(host(sa).view(np.uint32), sa_o.view(np.uint32))
+    assert np.array_equal(host(sb).view(np.uint32), sb_o.view(np.uint32))
+    o, m = oracle.gemm(qa_o, sa_o, qb_o, sb_o, bscale=bscale)
+    assert_gemm_close(host(d), o, m, ODT[out_dtype], f"random {M}x{N}x{K} row_b={row_b}")
