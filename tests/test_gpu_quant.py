@@ -222,3 +222,19 @@ def test_dual_full_wgrad_x(gpu_device):
     torch.cuda.synchronize()
     assert torch.equal(q_row, q0) and torch.equal(s_row.view(torch.int32), s0.view(torch.int32))
     assert torch.equal(q_col_t, q1) and torch.equal(s_col.view(torch.int32), s1.view(torch.int32))
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_random_shapes_all_quantizers(gpu_device, seed):
+    """Random shapes for every quantizer, bit for bit against the oracle:
+    1x128 with any row count, 128x1 with channel counts that are and are not
+    multiples of 128, the fused kernel, and 128x128 with its transposed copy."""
+    rng = np.random.default_rng(500 + seed)
+    rows_any = int(rng.integers(1, 700))
+    t128, c128 = int(rng.integers(1, 6)) * 128, int(rng.integers(1, 9)) * 128
+    c8 = int(rng.integers(1, 100)) * 8
+    _act_parity(synth.activations_random_outliers(rng, rows_any, c128), 0, gpu_device)
+    _act_parity(synth.gradients_token_outliers(rng, t128, c8), 1, gpu_device)
+    _act_parity(synth.gradients_token_outliers(rng, t128, c128), 1, gpu_device)
+    _dual_parity(synth.activations_channel_outliers(rng, t128, c128), gpu_device)
+    _w_parity(synth.master_weight(rng, t128, c128), gpu_device, transposed=bool(seed % 2))
