@@ -29,6 +29,9 @@ std::atomic<uint64_t> g_wait_limit_ns{kWaitLimitNs};
 std::mutex g_dev_mu;
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+// Scale arrays are read and written one float at a time (except the GEMM's
+// per-row B scales, which arrive by bulk copies): 4-byte alignment suffices.
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
 // Probe the current device once; returns a library status.
 int current_device(DeviceInfo** out) {
@@ -76,7 +79,7 @@ int fp8_quant_act_1x128(const void* x_bf16, int64_t rows, int64_t cols, int axis
     if (rows > (int64_t(1) << 40) / cols) return kErrInvalidArg;
     // the 1x128 kernel's grid: (rows / 64) blocks by (cols / 128) group columns
     if (axis == FP8FG_AXIS_COLS && (cols / 128 > 65535 || rows / 64 >= (int64_t(1) << 31))) return kErrInvalidArg;
-    if (!aligned16(x_bf16) || !aligned16(q) || !aligned16(scales)) return kErrMisaligned;
+    if (!aligned16(x_bf16) || !aligned16(q) || !aligned4(scales)) return kErrMisaligned;
     DeviceInfo* d = nullptr;
     int st = current_device(&d);
     if (st != kOk) return st;
@@ -92,7 +95,7 @@ int fp8_quant_act_dual(const void* x_bf16, int64_t rows, int64_t cols, uint8_t* 
     if (rows > (int64_t(1) << 40) / cols) return kErrInvalidArg;
     // grid: (rows / 128) x (cols / 128) tiles
     if (cols / 128 > 65535) return kErrInvalidArg;
-    if (!aligned16(x_bf16) || !aligned16(q_row) || !aligned16(s_row) || !aligned16(q_col_t) || !aligned16(s_col))
+    if (!aligned16(x_bf16) || !aligned16(q_row) || !aligned4(s_row) || !aligned16(q_col_t) || !aligned4(s_col))
         return kErrMisaligned;
     DeviceInfo* d = nullptr;
     int st = current_device(&d);
@@ -106,7 +109,7 @@ int fp8_quant_w_128x128(const float* w, int64_t rows, int64_t cols, uint8_t* q, 
     if (rows == 0 || cols == 0) return kOk;
     if (!w || !q || !scales) return kErrInvalidArg;
     if (rows > (int64_t(1) << 40) / cols) return kErrInvalidArg;
-    if (!aligned16(w) || !aligned16(q) || !aligned16(scales) || (q_t && !aligned16(q_t))) return kErrMisaligned;
+    if (!aligned16(w) || !aligned16(q) || !aligned4(scales) || (q_t && !aligned16(q_t))) return kErrMisaligned;
     DeviceInfo* d = nullptr;
     int st = current_device(&d);
     if (st != kOk) return st;
@@ -151,7 +154,8 @@ int fp8_gemm_blockscaled(const uint8_t* a, const float* sa, const uint8_t* b, co
     if (M == 0 || N == 0) return kOk;
     if (!d) return kErrInvalidArg;
     if (K > 0 && (!a || !sa || !b || !sb)) return kErrInvalidArg;
-    if (!aligned16(d) || (K > 0 && (!aligned16(a) || !aligned16(sa) || !aligned16(b) || !aligned16(sb))))
+    const bool sb_ok = bscale == FP8FG_BSCALE_ROW ? aligned16(sb) : aligned4(sb);
+    if (!aligned16(d) || (K > 0 && (!aligned16(a) || !aligned4(sa) || !aligned16(b) || !sb_ok)))
         return kErrMisaligned;
     GemmArgs g{};
     g.a = a;
@@ -181,7 +185,7 @@ int fp8_gemm_grouped(const uint8_t* a, const float* sa, const uint8_t* b, const 
     if (M_total == 0 || N == 0) return kOk;
     if (!d) return kErrInvalidArg;
     if (K > 0 && (!a || !sa || !b || !sb)) return kErrInvalidArg;
-    if (!aligned16(d) || (K > 0 && (!aligned16(a) || !aligned16(sa) || !aligned16(b) || !aligned16(sb))) ||
+    if (!aligned16(d) || (K > 0 && (!aligned16(a) || !aligned4(sa) || !aligned16(b) || !aligned4(sb))) ||
         (reinterpret_cast<uintptr_t>(group_offsets) & 3u))
         return kErrMisaligned;
     GemmArgs g{};

@@ -52,7 +52,7 @@ extern "C" {
 typedef enum {
     FP8FG_OK = 0,
     FP8FG_ERR_INVALID_ARG = 1,        /* null pointer, bad enum, negative or non-tiling shape */
-    FP8FG_ERR_MISALIGNED = 2,         /* a pointer is not 16-byte aligned */
+    FP8FG_ERR_MISALIGNED = 2,         /* a pointer breaks its alignment rule (16 bytes; 4 for scales) */
     FP8FG_ERR_UNSUPPORTED_DEVICE = 3, /* current device is not sm_103 */
     FP8FG_ERR_CUDA = 4,               /* a CUDA runtime/driver call or a launch failed */
     FP8FG_ERR_TIMEOUT = 5             /* (device status) a bounded wait ran out */
@@ -87,7 +87,8 @@ typedef enum {
  *     q[cols, rows] uint8, i.e. the codes TRANSPOSED (K-major for the Wgrad GEMM);
  *     scales[rows/128, cols] float32: scales[t*cols + j] belongs to the group
  *     x[128t .. 128t+127, j].
- * x, q and scales must be 16-byte aligned.  rows == 0 or cols == 0 is a no-op.
+ * x and q must be 16-byte aligned, scales 4-byte aligned.  rows == 0 or
+ * cols == 0 is a no-op.
  */
 int fp8_quant_act_1x128(const void *x_bf16, int64_t rows, int64_t cols, int axis,
                         uint8_t *q, float *scales, cudaStream_t stream);
@@ -105,8 +106,9 @@ int fp8_quant_act_1x128(const void *x_bf16, int64_t rows, int64_t cols, int axis
  *   x_bf16  [rows, cols] BF16, row-major, 16-byte aligned.
  *   q_row   [rows, cols] E4M3 codes;       s_row [cols/128, rows] FP32.
  *   q_col_t [cols, rows] E4M3 codes;       s_col [rows/128, cols] FP32.
- *   rows and cols multiples of 128, cols/128 <= 65535; all buffers 16-byte
- *   aligned and owned by the caller.  rows == 0 or cols == 0 is a no-op.
+ *   rows and cols multiples of 128, cols/128 <= 65535; x and the codes
+ *   16-byte aligned, the scales 4-byte aligned; all owned by the caller.
+ *   rows == 0 or cols == 0 is a no-op.
  * Errors: FP8FG_ERR_INVALID_ARG (shape, NULL), FP8FG_ERR_MISALIGNED,
  * FP8FG_ERR_UNSUPPORTED_DEVICE, FP8FG_ERR_CUDA (launch).
  */
@@ -124,7 +126,9 @@ int fp8_quant_act_dual(const void *x_bf16, int64_t rows, int64_t cols, uint8_t *
  *        (the K-major B operand of the Dgrad GEMM; a block's scale is the
  *        same in both orientations);
  *   scales[rows/128, cols/128] float32, row-major.
- * All pointers 16-byte aligned.  rows == 0 or cols == 0 is a no-op.
+ * w, q and q_t 16-byte aligned, scales 4-byte aligned (so that experts can be
+ * quantized one by one into slices of a [G, rows/128, cols/128] array).
+ * rows == 0 or cols == 0 is a no-op.
  */
 int fp8_quant_w_128x128(const float *w, int64_t rows, int64_t cols,
                         uint8_t *q, uint8_t *q_t, float *scales, cudaStream_t stream);
@@ -148,7 +152,9 @@ int fp8_quant_w_128x128(const float *w, int64_t rows, int64_t cols,
  *   d[M, N]: float32 (out_dtype FP8FG_OUT_F32) or bfloat16 rounded to
  *     nearest even (FP8FG_OUT_BF16).
  * Requires M % 128 == 0, N % 128 == 0, K % 128 == 0 (tokens are padded to
- * 128 by the caller); all pointers 16-byte aligned; sb strides >= 0.
+ * 128 by the caller); a, b and d 16-byte aligned, sa 4-byte aligned, sb
+ * 4-byte aligned for block scales and 16-byte aligned for per-row B scales
+ * (copied in bulk); sb strides >= 0.
  * K == 0 writes zeros.  M == 0 or N == 0 is a no-op.
  * Accuracy (tested): |d - o| <= 2^-16 * sum_k |a~ b~| for FP32 output, plus
  * one BF16 spacing of o for BF16 output, o being the exact sum of the
@@ -171,8 +177,9 @@ int fp8_gemm_blockscaled(const uint8_t *a, const float *sa,
  *     off[G] = M_total, every entry a multiple of 128 (groups padded with
  *     zero rows); empty groups allowed;
  *   d[M_total, N] float32 or bfloat16.
- * Requires M_total % 128 == 0, N % 128 == 0, K % 128 == 0, 1 <= G <= 4096.
- * Offsets that break these rules are detected on the device: the kernel
+ * Requires M_total % 128 == 0, N % 128 == 0, K % 128 == 0, 1 <= G <= 4096;
+ * a, b and d 16-byte aligned, sa and sb 4-byte aligned, group_offsets 4-byte
+ * aligned.  Offsets that break these rules are detected on the device: the kernel
  * records FP8FG_ERR_INVALID_ARG in the device status word and writes nothing.
  */
 int fp8_gemm_grouped(const uint8_t *a, const float *sa,

@@ -51,7 +51,15 @@ def lib(cuda_lib_path):
 
 
 A16 = 0x10000          # a 16-byte aligned fake address: never dereferenced (rejected before any launch)
+
+
+def _has_gpu() -> bool:
+    import torch
+    return torch.cuda.is_available()
+
 MIS = 0x10008          # an 8-byte aligned fake address
+MIS2 = 0x10002         # a 2-byte aligned fake address (bad even for a scale array)
+NOPROBE = (3, 4)       # arguments accepted; the device probe then fails (no GPU here)
 
 
 def test_quant_act_argument_checks(lib):
@@ -66,6 +74,9 @@ def test_quant_act_argument_checks(lib):
     assert f(A16, 4, 128, 0, A16, None, None) == 1
     assert f(MIS, 4, 128, 0, A16, A16, None) == 2          # misaligned
     assert f(A16, 4, 128, 0, MIS, A16, None) == 2
+    assert f(A16, 4, 128, 0, A16, MIS2, None) == 2         # scales need 4-byte alignment
+    if not _has_gpu():
+        assert f(A16, 4, 128, 0, A16, MIS, None) in NOPROBE   # ... and no more
     assert f(None, 0, 128, 0, None, None, None) == 0       # empty: no-op, nothing touched
     assert f(None, 4, 0, 0, None, None, None) == 0
 
@@ -75,7 +86,8 @@ def test_quant_dual_argument_checks(lib):
     assert f(A16, 128, 100, A16, A16, A16, A16, None) == 1        # cols not a multiple of 128
     assert f(A16, 100, 128, A16, A16, A16, A16, None) == 1        # rows not a multiple of 128
     assert f(A16, 128, 128, A16, A16, None, A16, None) == 1       # null output
-    assert f(A16, 128, 128, A16, A16, MIS, A16, None) == 2        # misaligned
+    assert f(A16, 128, 128, A16, A16, MIS, A16, None) == 2        # misaligned codes
+    assert f(A16, 128, 128, A16, MIS2, A16, A16, None) == 2       # misaligned scales
     assert f(None, 0, 128, None, None, None, None, None) == 0     # empty: no-op
 
 
@@ -85,6 +97,7 @@ def test_quant_w_argument_checks(lib):
     assert f(A16, 100, 128, A16, None, A16, None) == 1
     assert f(None, 128, 128, A16, None, A16, None) == 1
     assert f(A16, 128, 128, A16, MIS, A16, None) == 2      # misaligned transposed output
+    assert f(A16, 128, 128, A16, None, MIS2, None) == 2
     assert f(A16, 0, 128, None, None, None, None) == 0
 
 
@@ -102,7 +115,10 @@ def test_gemm_argument_checks(lib):
     assert call(od=7) == 1 and call(bscale=3) == 1
     assert call(sn=-1) == 1
     assert call(a=None) == 1 and call(sb=None) == 1 and call(d=None) == 1
-    assert call(a=MIS) == 2 and call(d=MIS) == 2 and call(sa=MIS) == 2
+    assert call(a=MIS) == 2 and call(d=MIS) == 2 and call(sa=MIS2) == 2 and call(sb=MIS2) == 2
+    assert call(bscale=1, sb=MIS) == 2                     # per-row B scales arrive by 16-byte bulk copies
+    if not _has_gpu():
+        assert call(sa=MIS) in NOPROBE and call(sb=MIS) in NOPROBE
     assert call(M=0, a=None, d=None) == 0                  # empty: no-op
     assert call(M=1 << 32) == 1                            # beyond the supported range
     g = lib.fp8_gemm_grouped

@@ -106,3 +106,33 @@ def test_grouped_bad_offsets_reported(gpu_device):
                             out_dtype=fb.FP8FG_OUT_F32)
     assert fb.fp8fg_last_device_status() == 0
     assert torch.count_nonzero(y).item() == 0
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_grouped_random(gpu_device, seed):
+    """Random expert counts (empty experts included), random N and K: the
+    whole output against the oracle, pad rows exactly zero."""
+    rng = np.random.default_rng(700 + seed)
+    G = int(rng.integers(1, 13))
+    counts = rng.integers(0, 400, G) * (rng.random(G) > 0.2)
+    padded = ((counts + 127) // 128) * 128
+    if padded.sum() == 0:
+        counts[0], padded[0] = 1, 128
+    offsets = np.zeros(G + 1, np.int32)
+    offsets[1:] = np.cumsum(padded)
+    N, K = int(rng.integers(1, 5)) * 128, int(rng.integers(1, 7)) * 128
+    x = synth.moe_tokens(rng, counts, padded, K)
+    w = np.stack([synth.master_weight(rng, N, K) for _ in range(G)])
+    qa, sa = fb.fp8_quant_act_1x128(dev_bf16(x, gpu_device))
+    qb, sb = _quant_experts_gpu(w, gpu_device)
+    y = fb.fp8_gemm_grouped(qa, sa, qb, sb, dev(offsets, gpu_device), out_dtype=fb.FP8FG_OUT_F32)
+    torch.cuda.synchronize()
+    qa_o, sa_o = oracle.quant_act(x)
+    qs = [oracle.quant_w(w[g]) for g in range(G)]
+    o, m = oracle.gemm_grouped(qa_o, sa_o, np.stack([q for q, _ in qs]), np.stack([s for _, s in qs]), offsets)
+    yh = host(y)
+    assert_gemm_close(yh, o, m, "f32", f"grouped random G={G} N={N} K={K}")
+    r = 0
+    for c, p in zip(counts, padded):
+        assert np.all(yh[r + c:r + p] == 0)
+        r += p
