@@ -259,7 +259,24 @@ def test_random_shapes_against_the_oracle(gpu_device, seed):
     rng = np.random.default_rng(1000 + seed)
     M, N, K = (int(rng.integers(1, 5)) * 128, int(rng.integers(1, 7)) * 128, int(rng.integers(1, 9)) * 128)
     row_b = bool(seed % 3 == 2)
+    dgrad_like = bool(seed % 3 == 1)
     out_dtype = F32 if seed % 2 else BF16
+    if dgrad_like:
+        # Dgrad-like: B is the transposed copy of a weight W[K, N], its block
+        # scales read through swapped strides
+        a_src = synth.gradients_token_outliers(rng, M, K)
+        w_src = synth.master_weight(rng, K, N)
+        qa, sa = fb.fp8_quant_act_1x128(dev_bf16(a_src, gpu_device))
+        _, qb, sb = fb.fp8_quant_w_128x128(dev(w_src, gpu_device), transposed=True)
+        d = fb.fp8_gemm_blockscaled(qa, sa, qb, sb, sb_strides=(1, N // 128), out_dtype=out_dtype)
+        qa_o, sa_o = oracle.quant_act(a_src)
+        _, sb_o, qb_o = oracle.quant_w(w_src, transposed=True)
+        torch.cuda.synchronize()
+        assert np.array_equal(host(qa), qa_o) and np.array_equal(host(qb), qb_o)
+        assert np.array_equal(host(sb).view(np.uint32), sb_o.view(np.uint32))
+        o, m = oracle.gemm(qa_o, sa_o, qb_o, sb_o, sb_strides=(1, N // 128))
+        assert_gemm_close(host(d), o, m, ODT[out_dtype], f"random dgrad-like {M}x{N}x{K}")
+        return
     if row_b:
         # Wgrad-like: both operands from token-axis groups (K = tokens)
         a_src = synth.gradients_token_outliers(rng, K, M)
