@@ -23,11 +23,18 @@
 //               into a ring of their own; everything completes on mbarriers;
 //   warp 1      MMA issuer (lane 0 issues, the warp waits): before reusing a
 //               TMEM buffer it takes the buffer back from the promotion
-//               warps on a named barrier (bar.sync), then 4 x
-//               tcgen05.mma.kind::f8f6f4 (K = 32 each) per chunk into one of
-//               two 256-column buffers, and commits to the stage's "empty"
-//               mbarrier and the buffer's "full" one;
-//   warps 2-3   idle;
+//               warps on a named barrier (bar.sync), learns from warp 2 on
+//               another named barrier that the chunk's operands have landed,
+//               then issues 4 x tcgen05.mma.kind::f8f6f4 (K = 32 each) per
+//               chunk into one of two 256-column buffers and commits to the
+//               stage's "empty" mbarrier and the buffer's "full" one.  The
+//               warp touches no shared memory in this loop: an mbarrier
+//               wait in the MMA-issuing warp measured 150-300 cycles per
+//               chunk even on a completed phase, idling the tensor pipe;
+//   warp 2      operand watcher: waits for each chunk's "full" mbarrier and
+//               meets the MMA warp on a named barrier (bar.red.or carries a
+//               failed wait);
+//   warp 3      idle;
 //   warps 4-11  promotion: wait for the buffer, tcgen05.ld 8 x 16 columns
 //               (the next load in flight while the previous 16 columns are
 //               scaled and added with packed FP32 FMAs), hand the buffer back
@@ -71,6 +78,10 @@ constexpr uint32_t B_BYTES = BN * BK;
 // to the MMA warp through barrier 1 + b (bar.arrive by them, bar.sync by the
 // whole MMA warp).
 constexpr int kRelThreads = 32 * (1 + EPI_WARPS);
+// Named barrier 1 + NBUF: the operand watcher (warp 2) and the MMA warp meet
+// on it once per chunk (bar.red.or: the watcher reports a failed wait).
+constexpr int kOpsBar = 1 + NBUF;
+constexpr int kOpsThreads = 64;
 // Limit of the promotion warps' wait for a chunk's commit (see run_epilogue):
 // far above the longest settable limit of the other waits.
 constexpr uint64_t kHandoffLimitNs = 3 * kMaxWaitLimitNs;
@@ -242,17 +253,13 @@ FP8FG_DEV void run_producer(Smem<kRowB>& sm, const CUtensorMap* tmap_a, const CU
     }
 }
 
-// ----------------------------------------------------------------- MMA ---
-// Whole warp; lane 0 issues.  Lock step with the promotion warps: before
-// chunk g (g >= 2) the warp takes the hand-back of chunk g-2 on the named
-// barrier of its buffer, and for every chunk, aborted or not, lane 0 commits
-// the buffer's "full" mbarrier (with no MMA after an abort the commit only
-// tracks the earlier ones).  A promotion warp arrives for chunk g only after
-// that commit, so no arrival can run ahead of the MMA warp's bar.sync, and
-// every bar.sync is matched by the 8 arrivals of a chunk already committed.
+// ------------------------------------------------------- operand watcher ---
+// Whole warp; lane 0 waits.  For every chunk, in the MMA warp's order, wait
+// for the stage's "full" mbarrier (skipped after a failed wait) and meet the
+// MMA warp on kOpsBar, passing whether this or an earlier wait failed.  Both
+// warps meet exactly once per chunk on every path, so neither runs ahead.
 template <int kRowB>
-FP8FG_DEV void run_mma(Smem<kRowB>& sm, uint32_t tmem_base, const Params& p, int64_t m_tiles, int64_t n_tiles,
-                       int64_t kb, int lane) {
+FP8FG_DEV void run_watch(Smem<kRowB>& sm, const Params& p, int64_t m_tiles, int64_t n_tiles, int64_t kb, int lane) {
     constexpr int ST = Smem<kRowB>::kStages;
     volatile int* abort_flag = &sm.abort_flag;
     uint32_t g = 0;
@@ -261,14 +268,39 @@ FP8FG_DEV void run_mma(Smem<kRowB>& sm, uint32_t tmem_base, const Params& p, int
     for (int64_t t = blockIdx.x; t < num_tiles; t += gridDim.x) {
         for (int64_t c = 0; c < kb; ++c, ++g) {
             const uint32_t s = g % ST, ph = (g / ST) & 1;
-            const uint32_t buf = g % NBUF;
-            if (g >= NBUF) named_sync<kRelThreads>(1 + static_cast<int>(buf));
             if (ok) {
                 bool f = true;
                 if (lane == 0)
                     f = mbar_wait_bounded(smem_u32(&sm.full[s]), ph, abort_flag, p.status, p.limit_ns, kErrTimeout);
                 ok = __shfl_sync(0xffffffffu, f, 0) != 0;
             }
+            named_sync_or<kOpsThreads>(kOpsBar, !ok);
+        }
+    }
+}
+
+// ----------------------------------------------------------------- MMA ---
+// Whole warp; lane 0 issues.  Lock step with the promotion warps: before
+// chunk g (g >= 2) the warp takes the hand-back of chunk g-2 on the named
+// barrier of its buffer, and for every chunk, aborted or not, lane 0 commits
+// the buffer's "full" mbarrier (with no MMA after an abort the commit only
+// tracks the earlier ones).  A promotion warp arrives for chunk g only after
+// that commit, so no arrival can run ahead of the MMA warp's bar.sync, and
+// every bar.sync is matched by the 8 arrivals of a chunk already committed.
+// The chunk's operands are reported by the watcher on kOpsBar.
+template <int kRowB>
+FP8FG_DEV void run_mma(Smem<kRowB>& sm, uint32_t tmem_base, const Params& p, int64_t m_tiles, int64_t n_tiles,
+                       int64_t kb, int lane) {
+    constexpr int ST = Smem<kRowB>::kStages;
+    uint32_t g = 0;
+    const int64_t num_tiles = m_tiles * n_tiles;
+    bool ok = true;   // warp-uniform
+    for (int64_t t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+        for (int64_t c = 0; c < kb; ++c, ++g) {
+            const uint32_t s = g % ST;
+            const uint32_t buf = g % NBUF;
+            if (g >= NBUF) named_sync<kRelThreads>(1 + static_cast<int>(buf));
+            if (named_sync_or<kOpsThreads>(kOpsBar, false)) ok = false;
             if (lane == 0) {
                 if (ok) {
                     tc_fence_after();
@@ -530,6 +562,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(REGS_LOW));
         if (warp == 0 && lane == 0) run_producer<kRowB>(sm, &tmap_a, &tmap_b, p, m_tiles, n_tiles, kb);
         if (warp == 1) run_mma<kRowB>(sm, tmem_base, p, m_tiles, n_tiles, kb, lane);
+        if (warp == 2) run_watch<kRowB>(sm, p, m_tiles, n_tiles, kb, lane);
     } else {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(REGS_HIGH));
         run_epilogue<kRowB>(sm, tmem_base, p, &tmap_d, m_tiles, n_tiles, kb, warp, lane);

@@ -85,6 +85,18 @@ template <int kThreads>
 FP8FG_DEV void named_sync(int id) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "n"(kThreads) : "memory");
 }
+// bar.red.or: a bar.sync that also returns the OR of `pred` over the
+// participating threads.
+template <int kThreads>
+FP8FG_DEV bool named_sync_or(int id, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.or.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(pred)), "r"(id), "n"(kThreads)
+        : "memory");
+    return r != 0;
+}
 
 // ----------------------------------------------------------------- TMA ---
 
