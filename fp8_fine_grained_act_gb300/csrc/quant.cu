@@ -113,39 +113,66 @@ FP8FG_DEV float group_amax_bf16(const uint4& v) {
 }
 
 // ------------------------------------------------------------ 1 x 128 ----
-// Grid (row blocks of 64, 128-column groups): a CTA owns 64 rows of one
-// group column c.  A half-warp owns one group (16 lanes x 8 BF16 = 256
-// bytes) and keeps kRowU groups' loads in flight; the CTA's 64 scales are
-// contiguous in scales[c * rows + r].
-constexpr int kRowU = 4;
-constexpr int kRowsPerCta = 16 * kRowU;
+// Grid (row blocks, 128-column groups): a CTA owns kRowsPerCta rows of one
+// group column c.  A lane quad owns one row's group (4 lanes x 32 BF16 = 256
+// bytes): lane j of the quad loads the group's 16-byte chunks j, j+4, j+8,
+// j+12, so each load instruction reads 64 contiguous bytes per row and each
+// store writes 32; the group maximum needs two shuffles, and the scale's
+// division and reciprocal are shared by 32 elements per lane.  A warp covers
+// 8 rows per step and keeps kRowU steps' loads in flight; the scales of
+// consecutive rows are contiguous in scales[c * rows + r].
+constexpr int kRowU = 2;
+constexpr int kRowsPerCta = 64 * kRowU;
+
+// Max |x| of the 128 BF16 values a lane quad holds (32 per lane), as in
+// group_amax_bf16.
+FP8FG_DEV float quad_amax_bf16(const uint4 (&v)[4]) {
+    uint32_t m = 0;
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+        m = __vmaxu2(m, __vmaxu2(__vmaxu2(v[k].x & 0x7FFF7FFFu, v[k].y & 0x7FFF7FFFu),
+                                 __vmaxu2(v[k].z & 0x7FFF7FFFu, v[k].w & 0x7FFF7FFFu)));
+    // xor < 4 stays inside the quad that owns the group
+    m = __vmaxu2(m, __shfl_xor_sync(0xffffffffu, m, 2));
+    m = __vmaxu2(m, __shfl_xor_sync(0xffffffffu, m, 1));
+    const uint32_t hi = m >> 16, lo = m & 0xFFFFu;
+    return __uint_as_float((hi > lo ? hi : lo) << 16);
+}
 
 __global__ void __launch_bounds__(256) quant_act_rows_kernel(const uint4* __restrict__ x, int64_t rows,
                                                              int64_t cols, uint2* __restrict__ q,
                                                              float* __restrict__ scales) {
     const int64_t c = blockIdx.y;
-    const int l16 = threadIdx.x & 15, hw = threadIdx.x >> 4;
-    const int64_t r0 = static_cast<int64_t>(blockIdx.x) * kRowsPerCta + hw;
-    uint4 v[kRowU];
+    const int j = threadIdx.x & 3;        // chunks j, j+4, j+8, j+12 of the group
+    const int rq = threadIdx.x >> 2;      // row of the quad within a 64-row step
+    const int64_t r0 = static_cast<int64_t>(blockIdx.x) * kRowsPerCta + rq;
+    uint4 v[kRowU][4];
 #pragma unroll
     for (int u = 0; u < kRowU; ++u) {
-        const int64_t r = r0 + 16 * u;
-        v[u] = make_uint4(0, 0, 0, 0);
-        if (r < rows) v[u] = __ldcs(x + (r * cols + c * kGroup) / 8 + l16);
+        const int64_t r = r0 + 64 * u;
+        const uint4* src = x + (r * cols + c * kGroup) / 8 + j;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            v[u][k] = make_uint4(0, 0, 0, 0);
+            if (r < rows) v[u][k] = __ldcs(src + 4 * k);
+        }
     }
 #pragma unroll
     for (int u = 0; u < kRowU; ++u) {
-        const int64_t r = r0 + 16 * u;
-        // xor < 16 stays inside the half-warp that owns the group
-        const float amax = group_amax_bf16(v[u]);
+        const int64_t r = r0 + 64 * u;
+        const float amax = quad_amax_bf16(v[u]);
         if (r >= rows) continue;
         const float s = __fdiv_rn(amax, 448.0f);
         const GroupScale gs(s);
-        uint2 out;
-        out.x = quant_quad_bf16(v[u].x, v[u].y, gs);
-        out.y = quant_quad_bf16(v[u].z, v[u].w, gs);
-        __stcs(q + (r * cols + c * kGroup) / 8 + l16, out);
-        if (l16 == 0) scales[c * rows + r] = s;
+        uint2* dst = q + (r * cols + c * kGroup) / 8 + j;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            uint2 out;
+            out.x = quant_quad_bf16(v[u][k].x, v[u][k].y, gs);
+            out.y = quant_quad_bf16(v[u][k].z, v[u][k].w, gs);
+            __stcs(dst + 4 * k, out);
+        }
+        if (j == 0) scales[c * rows + r] = s;
     }
 }
 
