@@ -34,10 +34,11 @@ def test_wait_times_out_and_reports(gpu_device):
 
 @pytest.mark.parametrize("bscale", [fb.FP8FG_BSCALE_BLOCK128, fb.FP8FG_BSCALE_ROW])
 def test_gemm_waits_run_out_and_the_kernel_ends(gpu_device, bscale):
-    """With a 1 ns limit the GEMM's producer, MMA and scale-ring waits give up
-    almost at once: every CTA must still end (the promotion warps keep their
-    lock step with the MMA warp), report FP8FG_ERR_TIMEOUT, and leave a
-    context in which the next call with the default limit is correct."""
+    """With a 1 ns limit the GEMM's producer, operand-watcher and scale-ring
+    waits give up almost at once: every CTA must still end (the watcher and
+    the promotion warps keep their lock step with the MMA warp), report
+    FP8FG_ERR_TIMEOUT, and leave a context in which the next call with the
+    default limit is correct."""
     M, N, K = 512, 1024, 4096
     rng = np.random.default_rng(11)
     a = torch.from_numpy(rng.integers(0, 0x7E, (M, K), dtype=np.uint8)).to(gpu_device)
