@@ -126,6 +126,12 @@ def test_gemm_argument_checks(lib):
     assert g(A16, A16, A16, A16, None, 4, A16, 1, 128, 128, 128, None) == 1      # no offsets
     assert g(A16, A16, A16, A16, A16 + 2, 4, A16, 1, 128, 128, 128, None) == 2   # offsets not 4-aligned
     assert g(A16, A16, A16, A16, A16, 4, A16, 1, 100, 128, 128, None) == 1
+    assert g(A16, A16, A16, A16, A16, 4097, A16, 1, 128, 128, 128, None) == 1    # G > 4096
+    assert g(A16, A16, A16, A16, A16, 4, A16, 7, 128, 128, 128, None) == 1       # bad output type
+    assert g(MIS, A16, A16, A16, A16, 4, A16, 1, 128, 128, 128, None) == 2       # misaligned codes
+    assert g(A16, A16, A16, MIS2, A16, 4, A16, 1, 128, 128, 128, None) == 2      # misaligned scales
+    assert g(A16, A16, A16, A16, A16, 4, MIS, 1, 128, 128, 128, None) == 2       # misaligned output
+    assert g(None, None, None, None, A16, 4, None, 1, 0, 128, 128, None) == 0    # empty: no-op
 
 
 def test_watchdog_argument_checks(lib):
