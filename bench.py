@@ -8,27 +8,30 @@ One step = one Fprop linear layer of the FP8 training path, computed online:
      BF16 output Y[4096, 18432].
 value = 2*M*N*K / step time (TFLOP/s of the whole step, quantizers included),
 aggregated over all ranks (each rank runs its own replica: weak scaling).
-The JSON line also carries the per-kernel breakdown (quantizer GB/s against
-HBM, GEMM TFLOP/s against the FP8 tensor peak), the roofline of the dominant
-kernel, an end-to-end number through the C ABI with host buffers, the SM
-clocks seen during the timed region, and the CPU oracle timed on a bounded
-sample of the same workload.
+
+The JSON line also carries, under "kernels", one keyed record per
+configuration of the path -- the Fprop step's own kernels, the tiny Fprop,
+Dgrad, Wgrad and the grouped MoE GEMM, each with its quantizers -- with the
+time, TFLOP/s or GB/s of every kernel and its fraction of the peak; the
+roofline of the dominant kernel; the fused dual quantizer; the measured FP8
+tensor rate (a probe of back-to-back MMAs); an end-to-end number through the
+C ABI with host buffers; the SM clocks seen while each measured block ran
+(every block lasts at least a second, so that nvidia-smi samples it under
+load); and the CPU oracle timed on a bounded sample of the same workload.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload fprop|tiny|dgrad|wgrad|grouped]
+                  [--workload fprop|tiny|dgrad|wgrad|grouped] [--configs all|none]
 
 For N > 1 launch with torchrun (one rank per GPU); rank 0 prints the line.
---workload other than fprop times the same kernels on the other GEMMs of
-the FP8 path (the tiny 256x256x512 Fprop; Dgrad dY[8192,2048] x
-W[2048,7168]; Wgrad dY^T X with X[8192,7168], token-axis groups; grouped MoE
-64 experts W_g[2048,7168] over 32768 tokens) on one GPU and prints a line of
-the same metric for it.
+The per-configuration records are single-GPU measurements, taken at N = 1.
+--workload other than fprop prints a line for that configuration alone.
 """
 from __future__ import annotations
 
 import argparse
 import hashlib
 import json
+import math
 import os
 import re
 import statistics
@@ -48,13 +51,19 @@ WORKLOAD = ("Fprop linear: X[4096,7168] bf16 N(0,1) with 8 fixed outlier channel
             "W[18432,7168] fp32 master N(0,0.02^2), quantized 128x128; Y = X W^T [4096,18432] bf16, "
             "FP32 promotion every 128 of K; seed 1")
 FLOPS = 2.0 * M * N * K
-ACT_BYTES = M * K * 2 + M * K + (K // 128) * M * 4                 # 3.031 B per element
-W_BYTES = N * K * 4 + N * K + (N // 128) * (K // 128) * 4         # 5.0002 B per element
-DUAL_BYTES = M * K * 2 + 2 * M * K + 2 * (K // 128) * M * 4        # 4.0625 B per element (one read, two outputs)
+ROW_B_PER_ELT = 2 + 1 + 4 / 128          # 1x128 or 128x1 quantizer: read BF16, write a code, a scale per 128
+W_B_PER_ELT = 4 + 1 + 4 / 16384          # 128x128 quantizer: read FP32, write a code, a scale per block
+DUAL_B_PER_ELT = 2 + 2 + 8 / 128         # 1x128 and 128x1 from one read: two codes, two scales per 128
+ACT_BYTES = M * K * ROW_B_PER_ELT
+W_BYTES = N * K * W_B_PER_ELT
 GEMM_MIN_BYTES = M * K + N * K + 4 * (M * K // 128 + N * K // 16384) + M * N * 2
-FP8_OVER_BF16 = 4.5 / 2.25          # nominal dense FP8 : BF16 tensor ratio
+FP8_OVER_BF16 = 4.5 / 2.25               # nominal dense FP8 : BF16 tensor ratio
+NOMINAL_FP8_TFLOPS = 4500.0              # GB300 dense FP8, nominal
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
-PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "gemm_blockscaled_fprop_4096x18432x7168.md")
+PROFILES = os.path.join(ROOT, "profiles")
+PROFILE_SUMMARY = os.path.join(PROFILES, "gemm_blockscaled_fprop_4096x18432x7168.md")
+L2_BYTES = 129 * 2 ** 20
+MMA_TILE_FLOPS = 2.0 * 128 * 256 * 128   # one K chunk of one 128 x 256 tile
 
 
 # --------------------------------------------------------------- helpers ---
@@ -93,6 +102,14 @@ def peaks():
         return FALLBACK["hbm_gbs"], FALLBACK["bf16_tflops"], "fallback"
 
 
+def rotations(bytes_per_set: float, floor: int = 1, cap: int = 8) -> int:
+    """Input sets to rotate through so that consecutive uses of one set are
+    separated by at least twice the L2 capacity of other inputs."""
+    if bytes_per_set <= 0:
+        return floor
+    return int(max(floor, min(cap, math.ceil(2 * L2_BYTES / bytes_per_set) + 1)))
+
+
 def gemm_source_sha() -> str:
     """Hash of the GEMM's code (gemm.cu + ptx.cuh) with // comments and blank
     lines left out, so that a comment edit does not orphan a profile."""
@@ -106,11 +123,11 @@ def gemm_source_sha() -> str:
     return h.hexdigest()[:16]
 
 
-def profiled_traffic():
-    """DRAM bytes per GEMM launch from the committed ncu summary, if it was
+def profiled_traffic(path: str | None = None):
+    """DRAM bytes per GEMM launch from a committed ncu summary, if it was
     taken on the current kernel source; else None."""
     try:
-        text = open(PROFILE_SUMMARY).read()
+        text = open(path or PROFILE_SUMMARY).read()
     except OSError:
         return None
     sha = re.search(r"kernel source sha256\[:16\]:\s*([0-9a-f]+)", text)
@@ -121,7 +138,7 @@ def profiled_traffic():
 
 
 class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+    """nvidia-smi samples of SM clock and throttle reasons during a measured block."""
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -129,6 +146,7 @@ class ClockSampler:
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
+        self.out = ""
 
     def __enter__(self):
         try:
@@ -141,7 +159,6 @@ class ClockSampler:
         return self
 
     def __exit__(self, *exc):
-        self.out = ""
         if self.proc is not None:
             time.sleep(0.15)
             self.proc.terminate()
@@ -152,26 +169,34 @@ class ClockSampler:
                 self.out, _ = self.proc.communicate()
 
     def summary(self):
-        rows = []
-        for line in (self.out or "").splitlines():
-            f = [v.strip() for v in line.split(",")]
-            if len(f) < 9:
-                continue
-            try:
-                rows.append({"sm": float(f[1]), "max": float(f[2]), "power": float(f[3]),
-                             "hw_slowdown": f[5], "hw_thermal": f[6], "sw_thermal": f[7], "sw_power_cap": f[8]})
-            except ValueError:
-                continue
-        if not rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"]}
-        busy = [r for r in rows if r["power"] > 200.0] or rows
-        reasons = []
-        for key, name in (("hw_slowdown", "hw_slowdown"), ("hw_thermal", "hw_thermal_slowdown"),
-                          ("sw_thermal", "sw_thermal_slowdown"), ("sw_power_cap", "sw_power_cap")):
-            if any(r[key].lower().startswith("active") for r in busy):
-                reasons.append(name)
-        return {"sm_mhz": statistics.median(r["sm"] for r in busy), "sm_max_mhz": max(r["max"] for r in rows),
-                "reasons": reasons, "samples": len(busy), "power_w_max": max(r["power"] for r in rows)}
+        return summarize_clocks(self.out)
+
+
+def summarize_clocks(text: str, busy_watts: float = 250.0):
+    """Median SM clock and throttle reasons over the samples taken under load
+    (power above ``busy_watts``; all samples if none is)."""
+    rows = []
+    for line in (text or "").splitlines():
+        f = [v.strip() for v in line.split(",")]
+        if len(f) < 9:
+            continue
+        try:
+            rows.append({"sm": float(f[1]), "max": float(f[2]), "power": float(f[3]),
+                         "hw_slowdown": f[5], "hw_thermal": f[6], "sw_thermal": f[7], "sw_power_cap": f[8]})
+        except ValueError:
+            continue
+    if not rows:
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"]}
+    busy = [r for r in rows if r["power"] > busy_watts]
+    use = busy or rows
+    reasons = []
+    for key, name in (("hw_slowdown", "hw_slowdown"), ("hw_thermal", "hw_thermal_slowdown"),
+                      ("sw_thermal", "sw_thermal_slowdown"), ("sw_power_cap", "sw_power_cap")):
+        if any(r[key].lower().startswith("active") for r in use):
+            reasons.append(name)
+    return {"sm_mhz": statistics.median(r["sm"] for r in use), "sm_max_mhz": max(r["max"] for r in rows),
+            "reasons": reasons, "samples": len(rows), "samples_under_load": len(busy),
+            "power_w_max": max(r["power"] for r in rows)}
 
 
 # ------------------------------------------------------------- oracle CPU ---
@@ -220,23 +245,296 @@ def run_reference(args):
 
 # ------------------------------------------------------------------ GPU ---
 
+def _gpu_setup(local: int):
+    import torch
+    from fp8_fine_grained_act_gb300 import binding as fb
+    from fp8_fine_grained_act_gb300 import build as fbuild
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py: no CUDA device; the FP8 path has no CPU fallback")
+    torch.cuda.set_device(local)
+    fbuild.build()
+    fb.load()
+    return torch.device("cuda", local)
+
+
+def timed_rounds(kernels, rounds: int, stream):
+    """Run `rounds` rounds of the kernels (list of (name, fn)), an event
+    between consecutive kernels; returns the mean ms of each kernel and the
+    wall ms of the whole block on the device."""
+    import torch
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(kernels) + 1)] for _ in range(rounds)]
+    for i in range(rounds):
+        ev[i][0].record(stream)
+        for j, (_, fn) in enumerate(kernels):
+            fn(i)
+            ev[i][j + 1].record(stream)
+    torch.cuda.synchronize()
+    per = [sum(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(rounds)) / rounds for j in range(len(kernels))]
+    return per, ev[0][0].elapsed_time(ev[-1][-1])
+
+
+def block_rounds(kernels, stream, seconds: float, warmup: int, cap: int = 20000) -> int:
+    """Rounds needed for a measured block of at least `seconds` of GPU time."""
+    import torch
+    for i in range(max(warmup, 3)):
+        for _, fn in kernels:
+            fn(i)
+    torch.cuda.synchronize()
+    _, ms = timed_rounds(kernels, 5, stream)
+    return int(min(cap, max(20, math.ceil(seconds * 1e3 / max(ms / 5, 1e-3)))))
+
+
+def probe_tensor_rate(fb, stream, target_ms: float = 40.0, repeats: int = 5):
+    """Measured FP8 tensor rate: the library's probe of back-to-back
+    128x256x32 kind::f8f6f4 MMAs, one CTA per SM; the best of `repeats`."""
+    import torch
+    chunks = 2000
+    ctas = fb.fp8fg_probe_mma_rate(chunks, stream=stream)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    fb.fp8fg_probe_mma_rate(chunks, stream=stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    chunks = int(max(2000, min(1 << 22, chunks * target_ms / max(e0.elapsed_time(e1), 1e-3))))
+    best = 0.0
+    for _ in range(repeats):
+        e0.record(stream)
+        fb.fp8fg_probe_mma_rate(chunks, stream=stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        best = max(best, ctas * chunks * MMA_TILE_FLOPS / (e0.elapsed_time(e1) * 1e-3) / 1e12)
+    if fb.fp8fg_last_device_status() != 0:
+        raise SystemExit("tensor-rate probe: device status not clean")
+    return {"tflops": best, "ctas": ctas, "chunks_per_cta": chunks,
+            "how": "one CTA per SM issuing back-to-back tcgen05.mma.kind::f8f6f4 128x256x32 (the GEMM's "
+                   "instruction and operand layout), no data movement or promotion; best of 5 launches"}
+
+
+class Peaks:
+    def __init__(self, probe=None):
+        self.hbm, self.bf16, self.src = peaks()
+        self.fp8 = self.bf16 * FP8_OVER_BF16
+        self.probe = probe["tflops"] if probe else None
+
+    def gemm(self, flops: float, ms: float, extra=None):
+        tf = flops / (ms * 1e-3) / 1e12
+        r = {"us": ms * 1e3, "TFLOP/s": tf, "frac_fp8_peak": tf / self.fp8,
+             "frac_nominal_fp8": tf / NOMINAL_FP8_TFLOPS}
+        if self.probe:
+            r["frac_tensor_probe"] = tf / self.probe
+        if extra:
+            r.update(extra)
+        return r
+
+    def quant(self, nbytes: float, ms: float):
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        return {"us": ms * 1e3, "GB/s": gbs, "frac_hbm": gbs / self.hbm}
+
+    def legend(self):
+        d = {"fp8_tflops": self.fp8, "fp8_source": f"{self.src} bf16 burst {self.bf16} TFLOP/s x {FP8_OVER_BF16} "
+                                                  "(FP8:BF16 nominal)",
+             "nominal_fp8_tflops": NOMINAL_FP8_TFLOPS, "hbm_gbs": self.hbm, "hbm_source": self.src}
+        if self.probe:
+            d["tensor_probe_tflops"] = self.probe
+        return d
+
+
+def measure_config(name: str, dev, stream, pk: Peaks, seconds: float, warmup: int):
+    """One configuration of the path: its quantizers and GEMM, repeated for
+    at least `seconds` of GPU time with rotated inputs, CUDA events between
+    kernels and nvidia-smi sampling the SM clocks.  Returns its record."""
+    import torch
+
+    from fp8_fine_grained_act_gb300 import binding as fb
+    from fp8_fine_grained_act_gb300 import synth
+    bf = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+    rec = {}
+    if name == "tiny":
+        d = synth.tiny_fprop(seed=0)
+        x, w = bf(d["x"]), torch.from_numpy(d["w"]).to(dev)
+        Mw, Kw = x.shape
+        Nw = w.shape[0]
+        qx = torch.empty((Mw, Kw), dtype=torch.uint8, device=dev)
+        sx = torch.empty((Kw // 128, Mw), dtype=torch.float32, device=dev)
+        qw = torch.empty((Nw, Kw), dtype=torch.uint8, device=dev)
+        sw = torch.empty((Nw // 128, Kw // 128), dtype=torch.float32, device=dev)
+        y = torch.empty((Mw, Nw), dtype=torch.float32, device=dev)
+        kernels = [("quant_act_1x128 X[256,512]", lambda i: fb.fp8_quant_act_1x128(x, q=qx, scales=sx, stream=stream)),
+                   ("quant_w_128x128 W[256,512]", lambda i: fb.fp8_quant_w_128x128(w, q=qw, scales=sw, stream=stream)),
+                   ("gemm_blockscaled 256x256x512 f32", lambda i: fb.fp8_gemm_blockscaled(
+                       qx, sx, qw, sw, out_dtype=fb.FP8FG_OUT_F32, d=y, stream=stream))]
+        nbytes = [Mw * Kw * ROW_B_PER_ELT, Nw * Kw * W_B_PER_ELT, None]
+        flops = 2.0 * Mw * Nw * Kw
+        workload = ("Tiny Fprop: X[256,512] N(0,1) with 0.1% of entries x100, W[256,512] N(0,0.02^2), fp32 out; "
+                    "seed 0 (launch-latency bound: two 128x256 tiles)")
+        sets = 1
+    elif name == "dgrad":
+        d = synth.dgrad(seed=2)
+        Mw, Kw = d["dy"].shape
+        Nw = d["w"].shape[1]
+        sets = rotations(Mw * Kw * 2 + Kw * Nw * 4)
+        dys = [bf(d["dy"]) for _ in range(sets)]
+        ws = [torch.from_numpy(d["w"]).to(dev) for _ in range(sets)]
+        del d
+        qdy = torch.empty((Mw, Kw), dtype=torch.uint8, device=dev)
+        sdy = torch.empty((Kw // 128, Mw), dtype=torch.float32, device=dev)
+        qw = torch.empty((Kw, Nw), dtype=torch.uint8, device=dev)
+        qwt = torch.empty((Nw, Kw), dtype=torch.uint8, device=dev)
+        sw = torch.empty((Kw // 128, Nw // 128), dtype=torch.float32, device=dev)
+        y = torch.empty((Mw, Nw), dtype=torch.bfloat16, device=dev)
+        kernels = [("quant_act_1x128 dY[8192,2048]", lambda i: fb.fp8_quant_act_1x128(
+                        dys[i % sets], q=qdy, scales=sdy, stream=stream)),
+                   ("quant_w_128x128 W[2048,7168] + transposed copy", lambda i: fb.fp8_quant_w_128x128(
+                       ws[i % sets], transposed=True, q=qw, q_t=qwt, scales=sw, stream=stream)),
+                   ("gemm_blockscaled dgrad 8192x7168x2048 bf16", lambda i: fb.fp8_gemm_blockscaled(
+                       qdy, sdy, qwt, sw, sb_strides=(1, Nw // 128), d=y, stream=stream))]
+        nbytes = [Mw * Kw * ROW_B_PER_ELT, Kw * Nw * (W_B_PER_ELT + 1), None]
+        flops = 2.0 * Mw * Nw * Kw
+        workload = ("Dgrad: dX[8192,7168] = dY[8192,2048] . W[2048,7168]; dY = N(0,1) x exp(N(0,2)) per token, "
+                    "quantized 1x128; W fp32 master quantized 128x128 with a transposed copy, block scales read "
+                    "transposed; bf16 out; seed 2")
+    elif name == "wgrad":
+        d = synth.wgrad(seed=3)
+        T, Mw = d["dy"].shape
+        Nw = d["x"].shape[1]
+        Kw = T
+        sets = rotations(T * Mw * 2 + T * Nw * 2)
+        dys = [bf(d["dy"]) for _ in range(sets)]
+        xs = [bf(d["x"]) for _ in range(sets)]
+        del d
+        qa = torch.empty((Mw, T), dtype=torch.uint8, device=dev)
+        sa = torch.empty((T // 128, Mw), dtype=torch.float32, device=dev)
+        qb = torch.empty((Nw, T), dtype=torch.uint8, device=dev)
+        sb = torch.empty((T // 128, Nw), dtype=torch.float32, device=dev)
+        y = torch.empty((Mw, Nw), dtype=torch.float32, device=dev)
+        kernels = [("quant_act_128x1 dY[8192,2048]", lambda i: fb.fp8_quant_act_1x128(
+                        dys[i % sets], axis=fb.FP8FG_AXIS_ROWS, q=qa, scales=sa, stream=stream)),
+                   ("quant_act_128x1 X[8192,7168]", lambda i: fb.fp8_quant_act_1x128(
+                       xs[i % sets], axis=fb.FP8FG_AXIS_ROWS, q=qb, scales=sb, stream=stream)),
+                   ("gemm_blockscaled wgrad 2048x7168x8192 per-row B scales f32", lambda i: fb.fp8_gemm_blockscaled(
+                       qa, sa, qb, sb, bscale=fb.FP8FG_BSCALE_ROW, out_dtype=fb.FP8FG_OUT_F32, d=y, stream=stream))]
+        nbytes = [T * Mw * ROW_B_PER_ELT, T * Nw * ROW_B_PER_ELT, None]
+        flops = 2.0 * Mw * Nw * Kw
+        workload = ("Wgrad: dW[2048,7168] = dY^T . X over 8192 tokens; dY as Dgrad, X as Fprop, both quantized in "
+                    "128-token x 1-channel groups (transposed codes); per-row B scales; fp32 out; seed 3")
+    elif name == "grouped":
+        d = synth.grouped_moe(seed=4)
+        G, Nw, Kw = d["w"].shape
+        x = bf(d["x"])
+        w = torch.from_numpy(d["w"].reshape(G * Nw, Kw)).to(dev)
+        off = torch.from_numpy(d["offsets"]).to(dev)
+        Mw = x.shape[0]
+        del d
+        sets = 1
+        qx = torch.empty((Mw, Kw), dtype=torch.uint8, device=dev)
+        sx = torch.empty((Kw // 128, Mw), dtype=torch.float32, device=dev)
+        qw = torch.empty((G * Nw, Kw), dtype=torch.uint8, device=dev)
+        sw = torch.empty((G * Nw // 128, Kw // 128), dtype=torch.float32, device=dev)
+        y = torch.empty((Mw, Nw), dtype=torch.bfloat16, device=dev)
+        qw3, sw3 = qw.view(G, Nw, Kw), sw.view(G, Nw // 128, Kw // 128)
+        kernels = [(f"quant_act_1x128 X_all[{Mw},7168]", lambda i: fb.fp8_quant_act_1x128(
+                        x, q=qx, scales=sx, stream=stream)),
+                   ("quant_w_128x128 64 experts W_g[2048,7168]", lambda i: fb.fp8_quant_w_128x128(
+                       w, q=qw, scales=sw, stream=stream)),
+                   (f"gemm_grouped {Mw}x2048x7168 bf16", lambda i: fb.fp8_gemm_grouped(
+                       qx, sx, qw3, sw3, off, d=y, stream=stream))]
+        nbytes = [Mw * Kw * ROW_B_PER_ELT, G * Nw * Kw * W_B_PER_ELT, None]
+        flops = 2.0 * Mw * Nw * Kw
+        gemm_bytes = Mw * Kw + G * Nw * Kw + 4 * (Mw * Kw // 128 + G * Nw * Kw // 16384) + Mw * Nw * 2
+        workload = (f"Grouped MoE Fprop: 64 experts W_g[2048,7168] fp32 N(0,0.02^2) quantized 128x128; "
+                    f"Dirichlet(1)/multinomial counts over 32768 tokens padded to 128 (M_total {Mw}), X N(0,1) "
+                    f"quantized 1x128; bf16 out; seed 4")
+    else:
+        raise ValueError(name)
+
+    rounds = block_rounds(kernels, stream, seconds, warmup)
+    with ClockSampler(dev.index or 0) as clk:
+        per, block_ms = timed_rounds(kernels, rounds, stream)
+    status = fb.fp8fg_last_device_status()
+    if status != 0:
+        raise SystemExit(f"{name}: device status {status}: {fb.fp8fg_status_string(status)}")
+    for (kname, _), t, nb in zip(kernels, per, nbytes):
+        if nb is None:
+            extra = {}
+            if name == "grouped":
+                t_roof = max(flops / (pk.fp8 * 1e12), gemm_bytes / (pk.hbm * 1e9))
+                extra = {"roofline_us": t_roof * 1e6, "frac_roofline": t_roof / (t * 1e-3),
+                         "roofline": "max(2MNK / FP8 peak, minimum bytes / HBM)"}
+            rec[kname] = pk.gemm(flops, t, extra)
+        else:
+            rec[kname] = pk.quant(nb, t)
+    rec["step"] = {"ms": sum(per), "TFLOP/s": flops / (sum(per) * 1e-3) / 1e12, "rounds": rounds,
+                   "block_ms": block_ms, "input_sets": sets,
+                   "l2": "inputs rotate over sets totalling > 2x L2" if sets > 1 else
+                         ("one set larger than L2" if name == "grouped" else "launch-bound, fits in L2")}
+    if name == "tiny":
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for _, fn in kernels:
+                fn(0)
+        for _ in range(10):
+            graph.replay()
+        torch.cuda.synchronize()
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = 2000
+        g0.record(stream)
+        for _ in range(reps):
+            graph.replay()
+        g1.record(stream)
+        torch.cuda.synchronize()
+        gms = g0.elapsed_time(g1) / reps
+        rec["step as one CUDA graph (3 kernels)"] = {"us": gms * 1e3, "TFLOP/s": flops / (gms * 1e-3) / 1e12}
+    rec["clocks"] = clk.summary()
+    rec["workload"] = workload
+    rec["M_N_K"] = [int(Mw), int(Nw), int(Kw)]
+    rec["gpu_launches"] = len(kernels) * rounds
+    return rec, flops, sum(per)
+
+
+def measure_dual(dev, stream, pk: Peaks, seconds: float):
+    """The fused 1x128 + 128x1 quantizer on X[4096,7168] and X[8192,7168]
+    (what a training forward runs to cache X in FP8 for the weight
+    gradient), inputs rotated over more than twice the L2."""
+    import torch
+
+    from fp8_fine_grained_act_gb300 import binding as fb
+    out = {}
+    for rows in (4096, 8192):
+        cols = 7168
+        sets = rotations(rows * cols * 2)
+        gen = torch.Generator(device=dev).manual_seed(5)
+        base = torch.randn((rows, cols), device=dev, generator=gen, dtype=torch.float32).to(torch.bfloat16)
+        xs = [base.clone() for _ in range(sets)]
+        qr = torch.empty((rows, cols), dtype=torch.uint8, device=dev)
+        sr = torch.empty((cols // 128, rows), dtype=torch.float32, device=dev)
+        qc = torch.empty((cols, rows), dtype=torch.uint8, device=dev)
+        sc = torch.empty((rows // 128, cols), dtype=torch.float32, device=dev)
+        kern = [("dual", lambda i: fb.fp8_quant_act_dual(xs[i % sets], q_row=qr, s_row=sr, q_col_t=qc, s_col=sc,
+                                                         stream=stream))]
+        rounds = block_rounds(kern, stream, seconds, 5)
+        with ClockSampler(dev.index or 0) as clk:
+            per, _ = timed_rounds(kern, rounds, stream)
+        r = pk.quant(rows * cols * DUAL_B_PER_ELT, per[0])
+        r.update({"rounds": rounds, "input_sets": sets, "clocks": clk.summary()})
+        out[f"quant_act_dual_1x128_128x1 X[{rows},{cols}]"] = r
+        del xs, base
+    if fb.fp8fg_last_device_status() != 0:
+        raise SystemExit("dual quantizer: device status not clean")
+    return out
+
+
 def run_gpu(args):
     import torch
     import torch.distributed as dist
 
     from fp8_fine_grained_act_gb300 import binding as fb
-    from fp8_fine_grained_act_gb300 import build as fbuild
     from fp8_fine_grained_act_gb300 import synth
 
     rank, world, local = dist_env()
-    if not torch.cuda.is_available():
-        raise SystemExit("bench.py: no CUDA device; the FP8 path has no CPU fallback")
-    torch.cuda.set_device(local)
+    dev = _gpu_setup(local)
     if world > 1:
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    fbuild.build()
-    fb.load()
-    dev = torch.device("cuda", local)
 
     d = synth.fprop_linear(seed=rank_seed(rank))
     x_h = torch.from_numpy(d["x"].view(np.int16)).view(torch.bfloat16).pin_memory()
@@ -270,19 +568,33 @@ def run_gpu(args):
     torch.cuda.synchronize()
     assert fb.fp8fg_last_device_status() == 0
 
+    # soak: the same step for at least --soak seconds right before the timed
+    # steps, so that the clock sampler sees the GPU under this load
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(5):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    soak_steps = int(max(1, math.ceil(args.soak * 1e3 / max(e0.elapsed_time(e1) / 5, 1e-3))))
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
     with ClockSampler(local) as clk:
+        e0.record(stream)
+        for _ in range(soak_steps):
+            step()
+        e1.record(stream)
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
         start.record(stream)
         for i in range(args.steps):
             step(evs[i])
         end.record(stream)
         torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
+        if world > 1:
+            dist.barrier()
+    soak_ms = e0.elapsed_time(e1) / soak_steps
     total_ms = start.elapsed_time(end)
     t_act = sum(e[0].elapsed_time(e[1]) for e in evs) / args.steps
     t_w = sum(e[1].elapsed_time(e[2]) for e in evs) / args.steps
@@ -302,7 +614,6 @@ def run_gpu(args):
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(e2e_steps):
         x.copy_(x_h, non_blocking=True)
@@ -355,32 +666,42 @@ def run_gpu(args):
     e2e_ms = max_over_ranks(p0.elapsed_time(p1) / e2e_steps)
     del xs[1], ws[1], ys[1], yhs[1]
 
-    # outside the step: the fused 1x128 + 128x1 quantizer on the same X (what a
-    # training forward runs to cache X in FP8 for the weight gradient)
-    qr, srw, qct, scl = fb.fp8_quant_act_dual(x, stream=stream)
-    dual_iters = 50
-    torch.cuda.synchronize()
-    e0.record(stream)
-    for _ in range(dual_iters):
-        fb.fp8_quant_act_dual(x, stream=stream)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    t_dual = max_over_ranks(e0.elapsed_time(e1) / dual_iters)
-    del qr, srw, qct, scl
-
     ms_step = max_over_ranks(total_ms / args.steps)
     t_gemm = max_over_ranks(t_gemm)
     t_act = max_over_ranks(t_act)
     t_w = max_over_ranks(t_w)
+    single = world == 1 and args.configs == "all"
+    probe = probe_tensor_rate(fb, stream) if single else None
+    pk = Peaks(probe)
+    kernels = {"fprop": {"quant_act_1x128 X[4096,7168]": pk.quant(ACT_BYTES, t_act),
+                         "quant_w_128x128 W[18432,7168]": pk.quant(W_BYTES, t_w),
+                         "gemm_blockscaled fprop 4096x18432x7168 bf16": pk.gemm(FLOPS, t_gemm),
+                         "step": {"ms": ms_step, "soak_ms_per_step": soak_ms, "soak_steps": soak_steps,
+                                  "l2": "inputs larger than L2: each step reads X (58.7 MB) and W (528 MB)"},
+                         "clocks": clk.summary()}}
+    launches = 3 * args.steps
+    if single:
+        del x_h, w_h, y_h, yhs
+        torch.cuda.empty_cache()
+        kernels.update(measure_dual(dev, stream, pk, args.block_seconds))
+        for name in ("tiny", "dgrad", "wgrad", "grouped"):
+            rec, _, _ = measure_config(name, dev, stream, pk, args.block_seconds, args.warmup)
+            kernels[name] = rec
+            torch.cuda.empty_cache()
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
         return
 
-    hbm, bf16, src = peaks()
-    fp8_peak = bf16 * FP8_OVER_BF16
     gemm_tflops = FLOPS / (t_gemm * 1e-3) / 1e12
-    clocks = clk.summary()
+    roof = {"bound": "tensor", "achieved": gemm_tflops, "peak": pk.fp8, "unit": "TFLOP/s",
+            "frac": gemm_tflops / pk.fp8, "traffic": profiled_traffic(),
+            "kernel": "gemm_blockscaled_kernel<0>",
+            "peak_source": f"{pk.src} bf16 burst {pk.bf16} TFLOP/s x {FP8_OVER_BF16} (FP8:BF16 nominal ratio)",
+            "frac_nominal_fp8": gemm_tflops / NOMINAL_FP8_TFLOPS}
+    if probe:
+        roof["frac_tensor_probe"] = gemm_tflops / probe["tflops"]
+        roof["tensor_probe_tflops"] = probe["tflops"]
     line = {
         "metric": METRIC,
         "value": world * FLOPS / (ms_step * 1e-3) / 1e12,
@@ -397,29 +718,19 @@ def run_gpu(args):
         "config": {"workload": WORKLOAD, "M": M, "N": N, "K": K,
                    "l2": "inputs larger than L2: each step reads X (58.7 MB) and W (528 MB)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
-        "roofline": {"bound": "tensor", "achieved": gemm_tflops, "peak": fp8_peak, "unit": "TFLOP/s",
-                     "frac": gemm_tflops / fp8_peak, "traffic": profiled_traffic(),
-                     "kernel": "gemm_blockscaled_kernel<0>",
-                     "peak_source": f"{src} bf16 burst {bf16} TFLOP/s x {FP8_OVER_BF16} (FP8:BF16 nominal)"},
-        "kernels": {
-            "quant_act_1x128": {"us": t_act * 1e3, "GB/s": ACT_BYTES / (t_act * 1e-3) / 1e9,
-                                "frac_hbm": ACT_BYTES / (t_act * 1e-3) / 1e9 / hbm},
-            "quant_w_128x128": {"us": t_w * 1e3, "GB/s": W_BYTES / (t_w * 1e-3) / 1e9,
-                                "frac_hbm": W_BYTES / (t_w * 1e-3) / 1e9 / hbm},
-            "quant_act_dual_1x128_128x1 (not in the step)": {
-                "us": t_dual * 1e3, "GB/s": DUAL_BYTES / (t_dual * 1e-3) / 1e9,
-                "frac_hbm": DUAL_BYTES / (t_dual * 1e-3) / 1e9 / hbm},
-            "gemm_blockscaled": {"us": t_gemm * 1e3, "TFLOP/s": gemm_tflops, "frac_fp8_peak": gemm_tflops / fp8_peak},
-            "hbm_peak_gbs": hbm, "hbm_peak_source": src,
-        },
+        "roofline": roof,
+        "kernels": kernels,
+        "peaks": pk.legend(),
         "e2e": {"value": world * FLOPS / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
-                "h2d_bytes_per_step": x_h.numel() * 2 + w_h.numel() * 4,
-                "d2h_bytes_per_step": y_h.numel() * 2, "ms_per_step": e2e_ms, "steps": e2e_steps,
+                "h2d_bytes_per_step": M * K * 2 + N * K * 4,
+                "d2h_bytes_per_step": M * N * 2, "ms_per_step": e2e_ms, "steps": e2e_steps,
                 "how": "copies of step i+1 (H2D) and i-1 (D2H) overlap step i's kernels on separate streams",
                 "serial_ms_per_step": e2e_serial_ms},
-        "gpu_launches": 3 * args.steps,
-        "clocks": clocks,
+        "gpu_launches": launches,
+        "clocks": clk.summary(),
     }
+    if probe:
+        line["tensor_probe"] = probe
     if not args.no_cpu_baseline:
         mb, nb = 1024, 4096
         v, cores, dt = cpu_baseline(mb, nb)
@@ -432,194 +743,36 @@ def run_gpu(args):
 
 
 def run_other(args):
-    """One step of another GEMM of the path (quantizers + GEMM), single GPU,
-    CUDA events per kernel; the line has the same metric and a per-kernel
-    breakdown."""
+    """One configuration alone (single GPU): a line of the same metric with
+    its per-kernel breakdown."""
     import torch
-
     from fp8_fine_grained_act_gb300 import binding as fb
-    from fp8_fine_grained_act_gb300 import build as fbuild
-    from fp8_fine_grained_act_gb300 import synth
-
-    if not torch.cuda.is_available():
-        raise SystemExit("bench.py: no CUDA device; the FP8 path has no CPU fallback")
-    fbuild.build()
-    fb.load()
-    dev = torch.device("cuda", 0)
-    bf = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
-    kernels = []   # (name, fn, algorithmic bytes or None)
-    extra = {}
-    if args.workload == "tiny":
-        d = synth.tiny_fprop(seed=0)
-        x, w = bf(d["x"]), torch.from_numpy(d["w"]).to(dev)
-        Mw, Kw = x.shape
-        Nw = w.shape[0]
-        qx = torch.empty((Mw, Kw), dtype=torch.uint8, device=dev)
-        sx = torch.empty((Kw // 128, Mw), dtype=torch.float32, device=dev)
-        qw = torch.empty((Nw, Kw), dtype=torch.uint8, device=dev)
-        sw = torch.empty((Nw // 128, Kw // 128), dtype=torch.float32, device=dev)
-        y = torch.empty((Mw, Nw), dtype=torch.float32, device=dev)
-
-        def k_act():
-            fb.fp8_quant_act_1x128(x, q=qx, scales=sx)
-
-        def k_w():
-            fb.fp8_quant_w_128x128(w, q=qw, scales=sw)
-
-        def k_gemm():
-            fb.fp8_gemm_blockscaled(qx, sx, qw, sw, out_dtype=fb.FP8FG_OUT_F32, d=y)
-
-        # the same three calls captured once in a CUDA graph and replayed:
-        # this shape is bound by launch overhead, which the graph removes
-        for fn in (k_act, k_w, k_gemm):
-            fn()
-        torch.cuda.synchronize()
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph):
-            k_act()
-            k_w()
-            k_gemm()
-        extra["graph"] = graph
-
-        kernels = [("quant_act_1x128 X", k_act, Mw * Kw * 3.031), ("quant_w_128x128 W", k_w, Nw * Kw * 5.0002),
-                   ("gemm_blockscaled", k_gemm, None)]
-        workload = ("Tiny Fprop: X[256,512] N(0,1) with 0.1% of entries x100, W[256,512] N(0,0.02^2), fp32 out; "
-                    "seed 0 (launch-latency bound: two 128x256 tiles)")
-    elif args.workload == "dgrad":
-        d = synth.dgrad(seed=2)
-        dy, w = bf(d["dy"]), torch.from_numpy(d["w"]).to(dev)
-        Mw, Kw = dy.shape
-        Nw = w.shape[1]
-        qdy = torch.empty((Mw, Kw), dtype=torch.uint8, device=dev)
-        sdy = torch.empty((Kw // 128, Mw), dtype=torch.float32, device=dev)
-        out = {}
-
-        def k_act():
-            fb.fp8_quant_act_1x128(dy, q=qdy, scales=sdy)
-
-        def k_w():
-            out["w"] = fb.fp8_quant_w_128x128(w, transposed=True)
-
-        k_w()
-        y = torch.empty((Mw, Nw), dtype=torch.bfloat16, device=dev)
-
-        def k_gemm():
-            fb.fp8_gemm_blockscaled(qdy, sdy, out["w"][1], out["w"][2], sb_strides=(1, Nw // 128), d=y)
-
-        kernels = [("quant_act_1x128 dY", k_act, Mw * Kw * 3.031),
-                   ("quant_w_128x128 W + transposed copy", k_w, Kw * Nw * 6.0002), ("gemm_blockscaled", k_gemm, None)]
-        workload = "Dgrad: dX[8192,7168] = dY[8192,2048] . W[2048,7168], block scales read transposed, bf16 out; seed 2"
-    elif args.workload == "wgrad":
-        d = synth.wgrad(seed=3)
-        dy, x = bf(d["dy"]), bf(d["x"])
-        T, Mw = dy.shape
-        Nw = x.shape[1]
-        Kw = T
-        res = {}
-
-        def k_dy():
-            res["a"] = fb.fp8_quant_act_1x128(dy, axis=fb.FP8FG_AXIS_ROWS)
-
-        def k_x():
-            res["b"] = fb.fp8_quant_act_1x128(x, axis=fb.FP8FG_AXIS_ROWS)
-
-        k_dy()
-        k_x()
-        y = torch.empty((Mw, Nw), dtype=torch.float32, device=dev)
-
-        def k_gemm():
-            fb.fp8_gemm_blockscaled(res["a"][0], res["a"][1], res["b"][0], res["b"][1], bscale=fb.FP8FG_BSCALE_ROW,
-                                    out_dtype=fb.FP8FG_OUT_F32, d=y)
-
-        kernels = [("quant_act_128x1 dY", k_dy, T * Mw * 3.031), ("quant_act_128x1 X", k_x, T * Nw * 3.031),
-                   ("gemm_blockscaled (per-row B scales)", k_gemm, None)]
-        workload = "Wgrad: dW[2048,7168] = dY^T . X over 8192 tokens, 128x1 groups, per-row B scales, fp32 out; seed 3"
-    else:
-        d = synth.grouped_moe(seed=4)
-        x = bf(d["x"])
-        G, Nw, Kw = d["w"].shape
-        w = torch.from_numpy(d["w"].reshape(G * Nw, Kw)).to(dev)
-        off = torch.from_numpy(d["offsets"]).to(dev)
-        Mw = x.shape[0]
-        del d
-        res = {}
-
-        def k_act():
-            res["a"] = fb.fp8_quant_act_1x128(x)
-
-        def k_w():
-            res["b"] = fb.fp8_quant_w_128x128(w, transposed=False)
-
-        k_act()
-        k_w()
-        y = torch.empty((Mw, Nw), dtype=torch.bfloat16, device=dev)
-
-        def k_gemm():
-            fb.fp8_gemm_grouped(res["a"][0], res["a"][1], res["b"][0].view(G, Nw, Kw),
-                                res["b"][1].view(G, Nw // 128, Kw // 128), off, d=y)
-
-        kernels = [("quant_act_1x128 X_all", k_act, Mw * Kw * 3.031),
-                   ("quant_w_128x128 64 experts", k_w, G * Nw * Kw * 5.0002), ("gemm_grouped", k_gemm, None)]
-        workload = (f"Grouped MoE Fprop: 64 experts W_g[2048,7168], Dirichlet(1)/multinomial counts over 32768 "
-                    f"tokens padded to 128 (M_total {Mw}); bf16 out; seed 4")
-    flops = 2.0 * Mw * Nw * Kw
-    for _ in range(args.warmup):
-        for _, fn, _ in kernels:
-            fn()
-    torch.cuda.synchronize()
-    assert fb.fp8fg_last_device_status() == 0
-    steps = min(args.steps, 200)
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(kernels) + 1)] for _ in range(steps)]
-    with ClockSampler(0) as clk:
-        for i in range(steps):
-            ev[i][0].record()
-            for j, (_, fn, _) in enumerate(kernels):
-                fn()
-                ev[i][j + 1].record()
-        torch.cuda.synchronize()
-    if fb.fp8fg_last_device_status() != 0:
-        raise SystemExit("device status not clean")
-    hbm, bf16, src = peaks()
-    fp8_peak = bf16 * FP8_OVER_BF16
-    per = [sum(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(steps)) / steps for j in range(len(kernels))]
-    ms = sum(per)
-    kd = {}
-    for (name, _, nbytes), t in zip(kernels, per):
-        if nbytes is None:
-            tf = flops / (t * 1e-3) / 1e12
-            kd[name] = {"us": t * 1e3, "TFLOP/s": tf, "frac_fp8_peak": tf / fp8_peak}
-        else:
-            kd[name] = {"us": t * 1e3, "GB/s": nbytes / (t * 1e-3) / 1e9, "frac_hbm": nbytes / (t * 1e-3) / 1e9 / hbm}
-    if "graph" in extra:
-        g = extra["graph"]
-        for _ in range(10):
-            g.replay()
-        torch.cuda.synchronize()
-        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        g0.record()
-        for _ in range(steps):
-            g.replay()
-        g1.record()
-        torch.cuda.synchronize()
-        graph_ms = g0.elapsed_time(g1) / steps
-        kd["step as one CUDA graph (3 kernels)"] = {"us": graph_ms * 1e3, "TFLOP/s": flops / (graph_ms * 1e-3) / 1e12}
-    line = {"metric": METRIC, "value": flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "n_gpus": 1, "steps": steps,
-            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "e4m3", "data": "synthetic",
-            "config": {"workload": workload, "M": Mw, "N": Nw, "K": Kw, "parallelism": "single GPU"},
-            "kernels": kd, "peaks": {"fp8_tflops": fp8_peak, "hbm_gbs": hbm, "source": src},
-            "clocks": clk.summary(), "gpu_launches": len(kernels) * steps}
+    dev = _gpu_setup(0)
+    stream = torch.cuda.current_stream()
+    pk = Peaks()
+    rec, flops, ms = measure_config(args.workload, dev, stream, pk, args.block_seconds, args.warmup)
+    line = {"metric": METRIC, "value": flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "n_gpus": 1,
+            "steps": rec["step"]["rounds"], "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "e4m3", "data": "synthetic",
+            "config": {"workload": rec["workload"], "M_N_K": rec["M_N_K"], "parallelism": "single GPU"},
+            "kernels": {args.workload: rec}, "peaks": pk.legend(), "clocks": rec["clocks"],
+            "gpu_launches": rec["gpu_launches"]}
+    del fb
     print(json.dumps(line), flush=True)
 
 
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", choices=["fprop", "tiny", "dgrad", "wgrad", "grouped"], default="fprop")
+    ap.add_argument("--configs", choices=["all", "none"], default="all",
+                    help="with the Fprop step, also measure the other configurations (N = 1 only)")
+    ap.add_argument("--soak", type=float, default=1.0, help="seconds of the Fprop step before the timed steps")
+    ap.add_argument("--block-seconds", type=float, default=1.0, help="GPU seconds of each configuration's block")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -25,6 +25,7 @@ FP8FG_ERR_MISALIGNED = 2
 FP8FG_ERR_UNSUPPORTED_DEVICE = 3
 FP8FG_ERR_CUDA = 4
 FP8FG_ERR_TIMEOUT = 5
+FP8FG_ERR_TEARDOWN = 6
 
 FP8FG_OUT_F32 = 0
 FP8FG_OUT_BF16 = 1
@@ -47,6 +48,7 @@ SIGNATURES = {
     "fp8fg_last_device_status": (_i32, [_vp]),
     "fp8fg_selftest_watchdog": (_i32, [_i64, _vp]),
     "fp8fg_set_wait_limit": (_i32, [_i64]),
+    "fp8fg_probe_mma_rate": (_i32, [_i64, ctypes.POINTER(ctypes.c_int), _vp]),
 }
 
 
@@ -105,10 +107,24 @@ def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
-def _need(t, dtype, shape, name):
-    if t.dtype != dtype or tuple(t.shape) != tuple(shape) or not t.is_contiguous() or not t.is_cuda:
-        raise ValueError(f"{name}: expected contiguous CUDA {dtype} {tuple(shape)}, got {t.dtype} "
-                         f"{tuple(t.shape)} on {t.device}")
+def _need(t, dtype, shape, name, device=None):
+    if (not isinstance(t, torch.Tensor) or t.dtype != dtype or tuple(t.shape) != tuple(shape)
+            or not t.is_contiguous() or not t.is_cuda):
+        got = f"{t.dtype} {tuple(t.shape)} on {t.device}" if isinstance(t, torch.Tensor) else type(t).__name__
+        raise ValueError(f"{name}: expected contiguous CUDA {dtype} {tuple(shape)}, got {got}")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name}: on {t.device}, the other operands on {device}")
+
+
+def _need_flat(t, dtype, min_numel, name, device):
+    """A contiguous CUDA array of at least ``min_numel`` elements (any shape):
+    the block scales of a GEMM read through strides."""
+    if (not isinstance(t, torch.Tensor) or t.dtype != dtype or not t.is_contiguous() or not t.is_cuda
+            or t.numel() < min_numel):
+        got = f"{t.dtype} {tuple(t.shape)} on {t.device}" if isinstance(t, torch.Tensor) else type(t).__name__
+        raise ValueError(f"{name}: expected a contiguous CUDA {dtype} array of >= {min_numel} elements, got {got}")
+    if t.device != device:
+        raise ValueError(f"{name}: on {t.device}, the other operands on {device}")
 
 
 # ------------------------------------------------------------ quantizers ---
@@ -128,23 +144,27 @@ def fp8_quant_act_1x128(x: torch.Tensor, axis: int = FP8FG_AXIS_COLS, q=None, sc
         q = torch.empty(qshape, dtype=torch.uint8, device=x.device)
     if scales is None:
         scales = torch.empty(sshape, dtype=torch.float32, device=x.device)
-    _need(q, torch.uint8, qshape, "q")
-    _need(scales, torch.float32, sshape, "scales")
+    _need(q, torch.uint8, qshape, "q", x.device)
+    _need(scales, torch.float32, sshape, "scales", x.device)
     st = load().fp8_quant_act_1x128(_ptr(x), rows, cols, int(axis), _ptr(q), _ptr(scales), _stream(stream))
     _check(st, "fp8_quant_act_1x128")
     return q, scales
 
 
-def fp8_quant_act_dual(x: torch.Tensor, stream=None):
+def fp8_quant_act_dual(x: torch.Tensor, q_row=None, s_row=None, q_col_t=None, s_col=None, stream=None):
     """BF16 x[rows, cols] -> (q_row, s_row, q_col_t, s_col) from one read of x:
     the outputs of fp8_quant_act_1x128 with axis 0 and with axis 1."""
     rows, cols = x.shape
     if x.dtype != torch.bfloat16 or not x.is_contiguous() or not x.is_cuda:
         raise ValueError("x must be a contiguous CUDA bfloat16 tensor")
-    q_row = torch.empty((rows, cols), dtype=torch.uint8, device=x.device)
-    s_row = torch.empty((cols // GROUP, rows), dtype=torch.float32, device=x.device)
-    q_col_t = torch.empty((cols, rows), dtype=torch.uint8, device=x.device)
-    s_col = torch.empty((rows // GROUP, cols), dtype=torch.float32, device=x.device)
+    shapes = {"q_row": ((rows, cols), torch.uint8), "s_row": ((cols // GROUP, rows), torch.float32),
+              "q_col_t": ((cols, rows), torch.uint8), "s_col": ((rows // GROUP, cols), torch.float32)}
+    given = {"q_row": q_row, "s_row": s_row, "q_col_t": q_col_t, "s_col": s_col}
+    for name, (shape, dt) in shapes.items():
+        if given[name] is None:
+            given[name] = torch.empty(shape, dtype=dt, device=x.device)
+        _need(given[name], dt, shape, name, x.device)
+    q_row, s_row, q_col_t, s_col = given["q_row"], given["s_row"], given["q_col_t"], given["s_col"]
     st = load().fp8_quant_act_dual(_ptr(x), rows, cols, _ptr(q_row), _ptr(s_row), _ptr(q_col_t), _ptr(s_col),
                                    _stream(stream))
     _check(st, "fp8_quant_act_dual")
@@ -163,10 +183,10 @@ def fp8_quant_w_128x128(w: torch.Tensor, transposed: bool = False, q=None, q_t=N
         q_t = torch.empty((cols, rows), dtype=torch.uint8, device=w.device)
     if scales is None:
         scales = torch.empty((rows // GROUP, cols // GROUP), dtype=torch.float32, device=w.device)
-    _need(q, torch.uint8, (rows, cols), "q")
-    _need(scales, torch.float32, (rows // GROUP, cols // GROUP), "scales")
+    _need(q, torch.uint8, (rows, cols), "q", w.device)
+    _need(scales, torch.float32, (rows // GROUP, cols // GROUP), "scales", w.device)
     if q_t is not None:
-        _need(q_t, torch.uint8, (cols, rows), "q_t")
+        _need(q_t, torch.uint8, (cols, rows), "q_t", w.device)
     st = load().fp8_quant_w_128x128(_ptr(w), rows, cols, _ptr(q), _ptr(q_t), _ptr(scales), _stream(stream))
     _check(st, "fp8_quant_w_128x128")
     return (q, q_t, scales) if transposed else (q, scales)
@@ -178,7 +198,7 @@ def _out(d, M, N, out_dtype, device):
     dt = torch.float32 if out_dtype == FP8FG_OUT_F32 else torch.bfloat16
     if d is None:
         d = torch.empty((M, N), dtype=dt, device=device)
-    _need(d, dt, (M, N), "d")
+    _need(d, dt, (M, N), "d", device)
     return d
 
 
@@ -187,15 +207,28 @@ def fp8_gemm_blockscaled(a, sa, b, sb, bscale: int = FP8FG_BSCALE_BLOCK128, sb_s
     """D[M,N] = A[M,K] . B[N,K]^T with group scales (see include/fp8fg.h).
     Block mode: sb_strides = (stride_n, stride_k) in elements, default
     (K/128, 1) for a row-major [N/128, K/128] array."""
+    if not isinstance(a, torch.Tensor) or a.dim() != 2 or not isinstance(b, torch.Tensor) or b.dim() != 2:
+        raise ValueError("a and b must be 2-D tensors [M, K] and [N, K]")
     M, K = a.shape
     N = b.shape[0]
     if b.shape[1] != K:
         raise ValueError("a and b disagree on K")
+    dev = a.device
+    _need(a, torch.uint8, (M, K), "a", dev)
+    _need(b, torch.uint8, (N, K), "b", dev)
+    _need(sa, torch.float32, (K // GROUP, M), "sa", dev)
     if bscale == FP8FG_BSCALE_BLOCK128:
         sn, sk = sb_strides if sb_strides is not None else (K // GROUP, 1)
-    else:
+        if sn < 0 or sk < 0:
+            raise ValueError("sb_strides must be non-negative")
+        last = (max(N // GROUP - 1, 0) * sn + max(K // GROUP - 1, 0) * sk + 1) if N and K else 0
+        _need_flat(sb, torch.float32, last, "sb", dev)
+    elif bscale == FP8FG_BSCALE_ROW:
         sn, sk = 0, 0
-    d = _out(d, M, N, out_dtype, a.device)
+        _need(sb, torch.float32, (K // GROUP, N), "sb", dev)
+    else:
+        raise ValueError(f"bscale {bscale}: expected FP8FG_BSCALE_BLOCK128 or FP8FG_BSCALE_ROW")
+    d = _out(d, M, N, out_dtype, dev)
     st = load().fp8_gemm_blockscaled(_ptr(a), _ptr(sa), _ptr(b), _ptr(sb), int(bscale), int(sn), int(sk),
                                      _ptr(d), int(out_dtype), M, N, K, _stream(stream))
     _check(st, "fp8_gemm_blockscaled")
@@ -205,13 +238,19 @@ def fp8_gemm_blockscaled(a, sa, b, sb, bscale: int = FP8FG_BSCALE_BLOCK128, sb_s
 def fp8_gemm_grouped(a, sa, b, sb, group_offsets, out_dtype: int = FP8FG_OUT_BF16, d=None, stream=None):
     """Grouped MoE GEMM: a[M_total, K], b[G, N, K], sb[G, N/128, K/128],
     group_offsets int32[G+1] on the device."""
+    if not isinstance(a, torch.Tensor) or a.dim() != 2 or not isinstance(b, torch.Tensor) or b.dim() != 3:
+        raise ValueError("a must be [M_total, K] and b [G, N, K]")
     M, K = a.shape
     G, N, Kb = b.shape
     if Kb != K:
         raise ValueError("a and b disagree on K")
-    if group_offsets.dtype != torch.int32 or not group_offsets.is_cuda or group_offsets.numel() != G + 1:
-        raise ValueError("group_offsets must be a CUDA int32 tensor of G+1 entries")
-    d = _out(d, M, N, out_dtype, a.device)
+    dev = a.device
+    _need(a, torch.uint8, (M, K), "a", dev)
+    _need(b, torch.uint8, (G, N, K), "b", dev)
+    _need(sa, torch.float32, (K // GROUP, M), "sa", dev)
+    _need(sb, torch.float32, (G, N // GROUP, K // GROUP), "sb", dev)
+    _need(group_offsets, torch.int32, (G + 1,), "group_offsets", dev)
+    d = _out(d, M, N, out_dtype, dev)
     st = load().fp8_gemm_grouped(_ptr(a), _ptr(sa), _ptr(b), _ptr(sb), _ptr(group_offsets), int(G), _ptr(d),
                                  int(out_dtype), M, N, K, _stream(stream))
     _check(st, "fp8_gemm_grouped")
@@ -233,3 +272,12 @@ def fp8fg_set_wait_limit(limit_ns: int) -> int:
 
 def fp8fg_status_string(status: int) -> str:
     return status_string(status)
+
+
+def fp8fg_probe_mma_rate(chunks: int, stream=None) -> int:
+    """Launch the tensor-rate probe (back-to-back FP8 MMAs, one CTA per SM)
+    on the stream; returns the number of CTAs.  Its FLOPs are
+    ctas * chunks * 2 * 128 * 256 * 128."""
+    n = ctypes.c_int(0)
+    _check(load().fp8fg_probe_mma_rate(int(chunks), ctypes.byref(n), _stream(stream)), "fp8fg_probe_mma_rate")
+    return int(n.value)

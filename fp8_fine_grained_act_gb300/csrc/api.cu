@@ -14,6 +14,15 @@ namespace {
 
 // Asynchronous errors recorded by kernels (bounded waits, grouped offsets).
 __device__ int g_device_status;
+// The value fp8fg_last_device_status took out of g_device_status, copied to
+// the host from here.
+__device__ int g_status_taken;
+
+// Read and clear the status word in one atomic step, so that a kernel on
+// another stream recording an error between a read and a separate clear
+// cannot have it wiped.
+__global__ void take_status_kernel() { g_status_taken = atomicExch(&g_device_status, 0); }
+std::mutex g_take_mu;   // g_status_taken is one word per device: one reader at a time
 
 constexpr int kMaxDevices = 64;
 
@@ -214,6 +223,8 @@ const char* fp8fg_status_string(int status) {
         case FP8FG_ERR_UNSUPPORTED_DEVICE: return "FP8FG_ERR_UNSUPPORTED_DEVICE: the current device is not sm_103";
         case FP8FG_ERR_CUDA: return "FP8FG_ERR_CUDA: a CUDA call or a kernel launch failed";
         case FP8FG_ERR_TIMEOUT: return "FP8FG_ERR_TIMEOUT: a bounded device wait ran out";
+        case FP8FG_ERR_TEARDOWN: return "FP8FG_ERR_TEARDOWN: after a failed wait, a kernel's wait for its own copies "
+                                        "or MMAs in flight also ran out before it released its resources";
         default: return "FP8FG: unknown status";
     }
 }
@@ -223,9 +234,11 @@ int fp8fg_last_device_status(cudaStream_t stream) {
     int st = current_device(&d);
     if (st != kOk) return st;
     int value = 0;
-    const int zero = 0;
-    if (cudaMemcpyAsync(&value, d->status_word, sizeof(int), cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
-        cudaMemcpyAsync(d->status_word, &zero, sizeof(int), cudaMemcpyHostToDevice, stream) != cudaSuccess ||
+    std::lock_guard<std::mutex> lock(g_take_mu);
+    take_status_kernel<<<1, 1, 0, stream>>>();
+    if (cudaPeekAtLastError() != cudaSuccess ||
+        cudaMemcpyFromSymbolAsync(&value, g_status_taken, sizeof(int), 0, cudaMemcpyDeviceToHost, stream) !=
+            cudaSuccess ||
         cudaStreamSynchronize(stream) != cudaSuccess)
         return kErrCuda;
     return value;
@@ -243,6 +256,16 @@ int fp8fg_selftest_watchdog(int64_t timeout_ns, cudaStream_t stream) {
     int st = current_device(&d);
     if (st != kOk) return st;
     return from_cuda(launch_watchdog_selftest(static_cast<uint64_t>(timeout_ns), d->status_word, stream));
+}
+
+int fp8fg_probe_mma_rate(int64_t chunks, int* num_ctas, cudaStream_t stream) {
+    if (chunks < 1 || chunks > (int64_t(1) << 24) || !num_ctas) return kErrInvalidArg;
+    DeviceInfo* d = nullptr;
+    int st = current_device(&d);
+    if (st != kOk) return st;
+    *num_ctas = d->num_sms;
+    return from_cuda(launch_mma_rate_probe(chunks, d->num_sms, g_wait_limit_ns.load(std::memory_order_relaxed),
+                                           d->status_word, stream));
 }
 
 }  // extern "C"

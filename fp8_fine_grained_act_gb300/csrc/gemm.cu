@@ -85,6 +85,9 @@ constexpr int kOpsThreads = 64;
 // Limit of the promotion warps' wait for a chunk's commit (see run_epilogue):
 // far above the longest settable limit of the other waits.
 constexpr uint64_t kHandoffLimitNs = 3 * kMaxWaitLimitNs;
+// Limit of the tear-down waits after a failure (copies in flight landing):
+// far above a copy's latency; running out records kErrTeardown.
+constexpr uint64_t kTeardownLimitNs = 10000000ull;
 
 // Shared memory.  kRowB = 1 (B scales per row of B) also keeps a ring of
 // the chunks' B scales.  (Three operand stages measured faster than four on
@@ -241,15 +244,19 @@ FP8FG_DEV void run_producer(Smem<kRowB>& sm, const CUtensorMap* tmap_a, const CU
         }
     }
     if (!ok) {
-        // abort: let the copies already issued land before the CTA exits
+        // abort: let the copies already issued land before the CTA exits; a
+        // copy still in flight after the limit is recorded as a tear-down
+        // failure (the CTA's shared memory is released with it pending)
+        bool landed = true;
         for (uint32_t s = 0; s < ST && s < g_ab; ++s) {
             const uint32_t last = s + ST * ((g_ab - 1 - s) / ST);
-            wait_plain(smem_u32(&sm.full[s]), (last / ST) & 1, 10000000ull);
+            landed &= wait_plain(smem_u32(&sm.full[s]), (last / ST) & 1, kTeardownLimitNs);
         }
         for (uint32_t s = 0; s < SL && s < g_sc; ++s) {
             const uint32_t last = s + SL * ((g_sc - 1 - s) / SL);
-            wait_plain(smem_u32(&sm.sfull[s]), (last / SL) & 1, 10000000ull);
+            landed &= wait_plain(smem_u32(&sm.sfull[s]), (last / SL) & 1, kTeardownLimitNs);
         }
+        if (!landed) atomicExch(p.status, kErrTeardown);
     }
 }
 
@@ -326,7 +333,7 @@ FP8FG_DEV void run_mma(Smem<kRowB>& sm, uint32_t tmem_base, const Params& p, int
     if (lane == 0) {
         // every MMA issued by this thread has finished before TMEM is released
         mma_commit(smem_u32(&sm.drain));
-        wait_plain(smem_u32(&sm.drain), 0, 100000000ull);
+        if (!wait_plain(smem_u32(&sm.drain), 0, 10 * kTeardownLimitNs)) atomicExch(p.status, kErrTeardown);
     }
     __syncwarp();
 }
@@ -700,6 +707,86 @@ __global__ void watchdog_kernel(uint64_t limit_ns, int* status) {
 
 cudaError_t launch_watchdog_selftest(uint64_t timeout_ns, int* status_word, cudaStream_t stream) {
     watchdog_kernel<<<1, 32, 0, stream>>>(timeout_ns, status_word);
+    return cudaPeekAtLastError();
+}
+
+// ------------------------------------------------ tensor-rate probe ---
+// The ceiling the block-scaled GEMM is measured against: one CTA per SM
+// issues `chunks` x 4 tcgen05.mma.kind::f8f6f4 of 128 x 256 x 32 back to back
+// (the GEMM's own instruction shape and operand layout, alternating between
+// two 256-column TMEM buffers), with no TMA, no promotion and no output.
+// The operands are a fixed pattern of finite E4M3 codes in shared memory.
+namespace {
+struct __align__(1024) ProbeSmem {
+    uint8_t a[A_BYTES];
+    uint8_t b[B_BYTES];
+    uint64_t done;
+    uint32_t tmem_base;
+    int abort_flag;
+};
+
+__global__ void __launch_bounds__(128, 1) mma_rate_kernel(int64_t chunks, uint64_t limit_ns, int* status) {
+    extern __shared__ uint8_t smem_raw[];
+    ProbeSmem& sm =
+        *reinterpret_cast<ProbeSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    uint32_t* words = reinterpret_cast<uint32_t*>(sm.a);
+    for (int i = threadIdx.x; i < static_cast<int>((A_BYTES + B_BYTES) / 4); i += blockDim.x)
+        words[i] = (0x31u * static_cast<uint32_t>(i) + 0x1234567u) & 0x77777777u;   // no NaN codes
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&sm.done), 1);
+        sm.abort_flag = 0;
+        fence_barrier_init();
+    }
+    fence_proxy_async_shared();
+    if (warp == 0) tmem_alloc(smem_u32(&sm.tmem_base), TMEM_COLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = sm.tmem_base;
+    if (warp == 0) {
+        if (lane == 0) {
+            const uint64_t adesc = smem_desc_sw128(smem_u32(sm.a));
+            const uint64_t bdesc = smem_desc_sw128(smem_u32(sm.b));
+            for (int64_t c = 0; c < chunks; ++c) {
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(c & 1) * BN;
+#pragma unroll
+                for (int kk = 0; kk < BK / MMA_K; ++kk) {
+                    const uint64_t koff = static_cast<uint64_t>((kk * MMA_K) >> 4);
+                    mma_f8f6f4(d_tmem, adesc + koff, bdesc + koff, kIdesc, kk > 0 ? 1u : 0u);
+                }
+            }
+            mma_commit(smem_u32(&sm.done));
+            if (!mbar_wait_bounded(smem_u32(&sm.done), 0, &sm.abort_flag, status, limit_ns, kErrTimeout)) {
+                // the MMAs must finish before TMEM is released
+                if (!wait_plain(smem_u32(&sm.done), 0, 10 * kTeardownLimitNs)) atomicExch(status, kErrTeardown);
+            }
+        }
+        __syncwarp();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) tmem_dealloc(tmem_base, TMEM_COLS);
+}
+std::once_flag g_probe_attr_once[64];
+}  // namespace
+
+cudaError_t launch_mma_rate_probe(int64_t chunks, int num_sms, uint64_t limit_ns, int* status_word,
+                                  cudaStream_t stream) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    // more than half of an SM's shared memory: one probe CTA per SM
+    const int smem = static_cast<int>(sizeof(ProbeSmem) + 1024) > 120 * 1024 ? static_cast<int>(sizeof(ProbeSmem) + 1024)
+                                                                                : 120 * 1024;
+    if (dev >= 0 && dev < 64) {
+        std::call_once(g_probe_attr_once[dev], [&] {
+            e = cudaFuncSetAttribute(mma_rate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        });
+        if (e != cudaSuccess) return e;
+    }
+    mma_rate_kernel<<<num_sms, 128, smem, stream>>>(chunks, limit_ns, status_word);
     return cudaPeekAtLastError();
 }
 

@@ -7,7 +7,15 @@
 namespace fp8fg {
 
 // Library status codes (mirror fp8fg_status of the public header).
-enum : int { kOk = 0, kErrInvalidArg = 1, kErrMisaligned = 2, kErrUnsupported = 3, kErrCuda = 4, kErrTimeout = 5 };
+enum : int {
+    kOk = 0,
+    kErrInvalidArg = 1,
+    kErrMisaligned = 2,
+    kErrUnsupported = 3,
+    kErrCuda = 4,
+    kErrTimeout = 5,
+    kErrTeardown = 6
+};
 
 // Bounded device waits give up after this long (nanoseconds) by default;
 // fp8fg_set_wait_limit() changes it within [1, kMaxWaitLimitNs].
@@ -44,5 +52,9 @@ struct GemmArgs {
 int launch_gemm(const GemmArgs& args, int num_sms, int* status_word, cudaStream_t stream, cudaError_t* cuda_err);
 
 cudaError_t launch_watchdog_selftest(uint64_t timeout_ns, int* status_word, cudaStream_t stream);
+
+// One CTA per SM issuing `chunks` x 4 back-to-back FP8 MMAs (128 x 256 x 32).
+cudaError_t launch_mma_rate_probe(int64_t chunks, int num_sms, uint64_t limit_ns, int* status_word,
+                                  cudaStream_t stream);
 
 }  // namespace fp8fg

@@ -3,8 +3,9 @@ training.  Shared by the tests, the benchmark and the smoke check; holds no
 quantization or GEMM arithmetic (only random draws and the BF16 rounding of
 the drawn FP32 values, which is how a BF16 activation tensor is produced).
 
-Distributions (the pages give the structure, the numbers are this library's
-choice, stated in the design notes):
+Distributions (the pages give the structure -- 4K-token sequences,
+activation outliers, token-correlated gradient outliers, MoE routing --
+but no parameters; the numbers below are this library's choice):
   * activations X ~ N(0, 1) with outliers, because fine-grained groups exist
     to contain activation outliers (DeepSeek-V3 FP8 post on innerforce.co.kr,
     fine-grained quantization paragraph): either a random 0.1 % of entries

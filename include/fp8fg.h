@@ -55,7 +55,10 @@ typedef enum {
     FP8FG_ERR_MISALIGNED = 2,         /* a pointer breaks its alignment rule (16 bytes; 4 for scales) */
     FP8FG_ERR_UNSUPPORTED_DEVICE = 3, /* current device is not sm_103 */
     FP8FG_ERR_CUDA = 4,               /* a CUDA runtime/driver call or a launch failed */
-    FP8FG_ERR_TIMEOUT = 5             /* (device status) a bounded wait ran out */
+    FP8FG_ERR_TIMEOUT = 5,            /* (device status) a bounded wait ran out */
+    FP8FG_ERR_TEARDOWN = 6            /* (device status) after a failed wait, the kernel's bounded wait for its
+                                         own TMA copies or MMAs in flight ran out too before it freed shared
+                                         and tensor memory; replaces an earlier FP8FG_ERR_TIMEOUT */
 } fp8fg_status;
 
 typedef enum { FP8FG_OUT_F32 = 0, FP8FG_OUT_BF16 = 1 } fp8fg_out_dtype;
@@ -194,8 +197,14 @@ const char *fp8fg_status_string(int status);
 /*
  * fp8fg_last_device_status -- read and clear the device status word of the
  * current device (an asynchronous error recorded by a kernel: a bounded
- * wait that ran out, or invalid grouped offsets).  Synchronises `stream`.
- * Returns FP8FG_OK when no kernel recorded anything since the last read.
+ * wait that ran out, or invalid grouped offsets).  The word is one per
+ * device, shared by every stream: the first error recorded since the last
+ * read wins (FP8FG_ERR_TEARDOWN overrides it).  The read and the clear are
+ * one atomic exchange on the device, ordered after the work already queued
+ * on `stream`; kernels queued on other streams are included only if the
+ * caller has ordered them before (synchronise those streams first).
+ * Synchronises `stream`.  Returns FP8FG_OK when no kernel recorded anything
+ * since the last read.
  */
 int fp8fg_last_device_status(cudaStream_t stream);
 
@@ -220,6 +229,20 @@ int fp8fg_set_wait_limit(int64_t limit_ns);
  * The caller reads it with fp8fg_last_device_status().  No fault, no trap.
  */
 int fp8fg_selftest_watchdog(int64_t timeout_ns, cudaStream_t stream);
+
+/*
+ * fp8fg_probe_mma_rate -- measurement hook: the tensor-core ceiling of the
+ * GEMM's own MMA.  Launches one CTA per SM (their number is written to
+ * *num_ctas), each issuing `chunks` (1 .. 2^24) x 4 back-to-back
+ * tcgen05.mma.kind::f8f6f4 of 128 x 256 x 32 on a fixed pattern of E4M3
+ * codes in shared memory, with no data movement, promotion or output.  The
+ * caller times the launch on `stream`; its work is
+ * *num_ctas * chunks * 2 * 128 * 256 * 128 FLOP.  The pages have no
+ * counterpart: it gives the block-scaled GEMM a measured denominator.  Its
+ * wait for the MMAs is bounded (fp8fg_set_wait_limit) and reports through
+ * the device status word.
+ */
+int fp8fg_probe_mma_rate(int64_t chunks, int *num_ctas, cudaStream_t stream);
 
 #ifdef __cplusplus
 }

@@ -35,11 +35,14 @@
  *     "Unified E4M3 format in DeepSeek-V3", section "Enhanced Numerical
  *     Stability").
  *
- * Readings taken where the pages are silent (each is listed in the design
- * notes): the element code is enc(fl32(x / s)) with an IEEE division, not a
- * multiply by a reciprocal; a group whose scale is 0 stores s = 0 and codes
- * that keep only the sign of x; NaN input encodes to 0x7F with its sign bit
- * (parity unpinned: inputs are finite by precondition).
+ * Readings taken where the pages are silent: the element code is
+ * enc(fl32(x / s)) with an IEEE single division (the pages give only
+ * "scale = amax / 448" and the quantize step; a multiply by a reciprocal
+ * and x * fl(448 / amax) differ from it in the last bit on rare inputs);
+ * a group whose scale is 0 (all zeros, or amax / 448 underflowing in FP32)
+ * stores s = 0 and codes that keep only the sign of x, so it dequantizes to
+ * zero; NaN input encodes to 0x7F with its sign bit (parity unpinned:
+ * inputs are finite by precondition).
  *
  * Build: gcc -O2 -std=c11 -fPIC -shared -fopenmp -ffp-contract=off
  *        -fno-fast-math (no FMA contraction, IEEE single division).

@@ -39,7 +39,7 @@ def test_library_exports_every_declared_symbol(cuda_lib_path):
 def test_status_strings(cuda_lib_path):
     from fp8_fine_grained_act_gb300 import binding as b
     for code, word in [(0, "OK"), (1, "INVALID_ARG"), (2, "MISALIGNED"), (3, "UNSUPPORTED"), (4, "CUDA"),
-                       (5, "TIMEOUT")]:
+                       (5, "TIMEOUT"), (6, "TEARDOWN")]:
         assert word in b.status_string(code)
     assert "unknown" in b.status_string(99)
 
@@ -171,3 +171,38 @@ def test_binding_rejects_host_tensors_before_any_call(lib):
         b.fp8_quant_act_1x128(torch.zeros((128, 128), dtype=torch.float32))
     with pytest.raises(ValueError):
         b._need(torch.zeros((4, 4)), torch.float32, (4, 4), "d")    # right dtype and shape, not on a GPU
+
+
+def test_gemm_bindings_check_every_operand_before_any_call(lib):
+    """Both GEMM bindings refuse host, mistyped, misshaped or non-contiguous
+    operands and undersized scale arrays with ValueError before the C ABI is
+    reached: a raw pointer to host memory or past the end of a scale array
+    must never reach a TMA load or a scale read on the device."""
+    import torch
+    from fp8_fine_grained_act_gb300 import binding as b
+    M, N, K = 128, 256, 256
+    a = torch.zeros((M, K), dtype=torch.uint8)
+    bb = torch.zeros((N, K), dtype=torch.uint8)
+    sa = torch.zeros((K // 128, M), dtype=torch.float32)
+    sb = torch.zeros((N // 128, K // 128), dtype=torch.float32)
+    with pytest.raises(ValueError):                                   # host operands
+        b.fp8_gemm_blockscaled(a, sa, bb, sb)
+    with pytest.raises(ValueError):                                   # mistyped A
+        b.fp8_gemm_blockscaled(a.float(), sa, bb, sb)
+    with pytest.raises(ValueError):                                   # non-contiguous B
+        b.fp8_gemm_blockscaled(a, sa, torch.zeros((K, N), dtype=torch.uint8).t(), sb)
+    with pytest.raises(ValueError):                                   # bad bscale enum
+        b.fp8_gemm_blockscaled(a, sa, bb, sb, bscale=5)
+    with pytest.raises(ValueError):                                   # negative strides
+        b.fp8_gemm_blockscaled(a, sa, bb, sb, sb_strides=(-1, 1))
+    G = 2
+    off = torch.tensor([0, 128, 128], dtype=torch.int32)
+    with pytest.raises(ValueError):
+        b.fp8_gemm_grouped(a, sa, torch.zeros((G, N, K), dtype=torch.uint8),
+                           torch.zeros((G, N // 128, K // 128)), off)
+    with pytest.raises(ValueError):                                   # B not [G, N, K]
+        b.fp8_gemm_grouped(a, sa, bb, sb, off)
+    # the size rule of a strided block-scale array: the last index read is
+    # (N/128 - 1) * stride_n + (K/128 - 1) * stride_k
+    with pytest.raises(ValueError):
+        b._need_flat(torch.zeros(3), torch.float32, 4, "sb", torch.device("cpu"))
