@@ -273,6 +273,48 @@ def timed_rounds(kernels, rounds: int, stream):
     return per, ev[0][0].elapsed_time(ev[-1][-1])
 
 
+class L2Flush:
+    """Reads a buffer of 3x the L2 capacity (a reduction, no writes): the L2
+    then holds only clean lines of it, so the kernel timed next starts with
+    cold inputs and with no dirty lines of earlier kernels left to write
+    back (a flush by writing would leave its own dirty lines instead)."""
+
+    def __init__(self, dev):
+        import torch
+        self.buf = torch.ones(3 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+        self.sink = torch.empty((), dtype=torch.float32, device=dev)
+
+    def __call__(self):
+        import torch
+        torch.amax(self.buf, dim=0, out=self.sink)
+
+
+def isolated_times(kernels, flush: L2Flush, stream, seconds: float):
+    """Each kernel alone: repeated launches, each after a read-only L2 flush,
+    CUDA events around the kernel only.  Returns the mean ms per kernel."""
+    import torch
+    out = []
+    for _, fn in kernels:
+        fn(0)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(5):
+            fn(i)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        reps = int(min(2000, max(20, math.ceil(seconds * 1e3 / (e0.elapsed_time(e1) / 5 + 0.05)))))
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        for i in range(reps):
+            flush()
+            ev[i][0].record(stream)
+            fn(i)
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        out.append(statistics.median(a.elapsed_time(b) for a, b in ev))
+    return out
+
+
 def block_rounds(kernels, stream, seconds: float, warmup: int, cap: int = 20000) -> int:
     """Rounds needed for a measured block of at least `seconds` of GPU time."""
     import torch
@@ -340,10 +382,13 @@ class Peaks:
         return d
 
 
-def measure_config(name: str, dev, stream, pk: Peaks, seconds: float, warmup: int):
+def measure_config(name: str, dev, stream, pk: Peaks, seconds: float, warmup: int, flush=None):
     """One configuration of the path: its quantizers and GEMM, repeated for
     at least `seconds` of GPU time with rotated inputs, CUDA events between
-    kernels and nvidia-smi sampling the SM clocks.  Returns its record."""
+    kernels and nvidia-smi sampling the SM clocks (the step as training runs
+    it: each kernel's time includes the write-back of what the previous one
+    left dirty in L2); then each kernel alone after a read-only L2 flush (its
+    own roofline).  Returns its record."""
     import torch
 
     from fp8_fine_grained_act_gb300 import binding as fb
@@ -454,7 +499,8 @@ def measure_config(name: str, dev, stream, pk: Peaks, seconds: float, warmup: in
     status = fb.fp8fg_last_device_status()
     if status != 0:
         raise SystemExit(f"{name}: device status {status}: {fb.fp8fg_status_string(status)}")
-    for (kname, _), t, nb in zip(kernels, per, nbytes):
+    alone = isolated_times(kernels, flush, stream, min(seconds, 0.5)) if flush is not None else [None] * len(kernels)
+    for (kname, _), t, ta, nb in zip(kernels, per, alone, nbytes):
         if nb is None:
             extra = {}
             if name == "grouped":
@@ -462,17 +508,25 @@ def measure_config(name: str, dev, stream, pk: Peaks, seconds: float, warmup: in
                 extra = {"roofline_us": t_roof * 1e6, "frac_roofline": t_roof / (t * 1e-3),
                          "roofline": "max(2MNK / FP8 peak, minimum bytes / HBM)"}
             rec[kname] = pk.gemm(flops, t, extra)
+            if ta is not None:
+                rec[kname]["alone"] = pk.gemm(flops, ta)
         else:
             rec[kname] = pk.quant(nb, t)
+            if ta is not None:
+                rec[kname]["alone"] = pk.quant(nb, ta)
     rec["step"] = {"ms": sum(per), "TFLOP/s": flops / (sum(per) * 1e-3) / 1e12, "rounds": rounds,
                    "block_ms": block_ms, "input_sets": sets,
                    "l2": "inputs rotate over sets totalling > 2x L2" if sets > 1 else
                          ("one set larger than L2" if name == "grouped" else "launch-bound, fits in L2")}
     if name == "tiny":
+        # the same three calls captured on the capture stream and replayed
         graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph):
-            for _, fn in kernels:
-                fn(0)
+        cap = torch.cuda.Stream()
+        cap.wait_stream(stream)
+        with torch.cuda.graph(graph, stream=cap):
+            fb.fp8_quant_act_1x128(x, q=qx, scales=sx, stream=cap)
+            fb.fp8_quant_w_128x128(w, q=qw, scales=sw, stream=cap)
+            fb.fp8_gemm_blockscaled(qx, sx, qw, sw, out_dtype=fb.FP8FG_OUT_F32, d=y, stream=cap)
         for _ in range(10):
             graph.replay()
         torch.cuda.synchronize()
@@ -681,11 +735,21 @@ def run_gpu(args):
                          "clocks": clk.summary()}}
     launches = 3 * args.steps
     if single:
+        flush = L2Flush(dev)
+        fk = [("a", lambda i: fb.fp8_quant_act_1x128(x, q=qx, scales=sx, stream=stream)),
+              ("w", lambda i: fb.fp8_quant_w_128x128(w, q=qw, scales=sw, stream=stream)),
+              ("g", lambda i: fb.fp8_gemm_blockscaled(qx, sx, qw, sw, out_dtype=fb.FP8FG_OUT_BF16, d=y,
+                                                      stream=stream))]
+        ta, tw, tg = isolated_times(fk, flush, stream, 0.5)
+        f = kernels["fprop"]
+        f["quant_act_1x128 X[4096,7168]"]["alone"] = pk.quant(ACT_BYTES, ta)
+        f["quant_w_128x128 W[18432,7168]"]["alone"] = pk.quant(W_BYTES, tw)
+        f["gemm_blockscaled fprop 4096x18432x7168 bf16"]["alone"] = pk.gemm(FLOPS, tg)
         del x_h, w_h, y_h, yhs
         torch.cuda.empty_cache()
         kernels.update(measure_dual(dev, stream, pk, args.block_seconds))
         for name in ("tiny", "dgrad", "wgrad", "grouped"):
-            rec, _, _ = measure_config(name, dev, stream, pk, args.block_seconds, args.warmup)
+            rec, _, _ = measure_config(name, dev, stream, pk, args.block_seconds, args.warmup, flush)
             kernels[name] = rec
             torch.cuda.empty_cache()
     if rank != 0:
@@ -750,7 +814,8 @@ def run_other(args):
     dev = _gpu_setup(0)
     stream = torch.cuda.current_stream()
     pk = Peaks()
-    rec, flops, ms = measure_config(args.workload, dev, stream, pk, args.block_seconds, args.warmup)
+    rec, flops, ms = measure_config(args.workload, dev, stream, pk, args.block_seconds, args.warmup,
+                                    L2Flush(dev) if args.alone else None)
     line = {"metric": METRIC, "value": flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "n_gpus": 1,
             "steps": rec["step"]["rounds"], "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "e4m3", "data": "synthetic",
@@ -773,6 +838,8 @@ def main(argv=None):
                     help="with the Fprop step, also measure the other configurations (N = 1 only)")
     ap.add_argument("--soak", type=float, default=1.0, help="seconds of the Fprop step before the timed steps")
     ap.add_argument("--block-seconds", type=float, default=1.0, help="GPU seconds of each configuration's block")
+    ap.add_argument("--alone", action="store_true",
+                    help="with --workload: also time each kernel alone after an L2 flush")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
