@@ -21,25 +21,24 @@
 //               per K chunk into a 3-stage shared-memory ring (128-byte
 //               swizzle) and, for per-row B scales, the chunk's B scales
 //               into a ring of their own; everything completes on mbarriers;
-//   warp 1      MMA issuer (lane 0 issues, the warp waits): per chunk one
-//               named barrier (bar.sync) on which the promotion warps hand
-//               back the TMEM buffer and warp 2 reports that the chunk's
-//               operands have landed; then 4 x tcgen05.mma.kind::f8f6f4
-//               (K = 32 each) into one of two 256-column buffers and ONE
-//               commit, to the chunk's "done" mbarrier, on which both the
-//               producer (stage free) and the promotion warps (partial sums
-//               ready) wait.  The warp touches no mbarrier in this loop: an
-//               mbarrier wait in the MMA-issuing warp measured 150-300
-//               cycles per chunk even on a completed phase, a second commit
-//               per chunk about 150, each idling the tensor pipe;
+//   warp 1      MMA issuer (lane 0 issues, the warp waits): before reusing a
+//               TMEM buffer it takes the buffer back from the promotion
+//               warps on a named barrier (bar.sync), learns from warp 2 on
+//               another named barrier that the chunk's operands have landed,
+//               then issues 4 x tcgen05.mma.kind::f8f6f4 (K = 32 each) per
+//               chunk into one of two 256-column buffers and commits to the
+//               stage's "empty" mbarrier and the buffer's "full" one.  The
+//               warp touches no shared memory in this loop: an mbarrier
+//               wait in the MMA-issuing warp measured 150-300 cycles per
+//               chunk even on a completed phase, idling the tensor pipe;
 //   warp 2      operand watcher: waits for each chunk's "full" mbarrier and
-//               arrives on the chunk's named barrier;
+//               meets the MMA warp on a named barrier (bar.red.or carries a
+//               failed wait);
 //   warp 3      idle;
 //   warps 4-11  promotion: wait for the buffer, tcgen05.ld 8 x 16 columns
 //               (the next load in flight while the previous 16 columns are
 //               scaled and added with packed FP32 FMAs), hand the buffer back
-//               (bar.arrive on the named barrier of the chunk two ahead),
-//               and after the tile's last chunk write the
+//               (bar.arrive), and after the tile's last chunk write the
 //               128 x 256 outputs through shared memory with TMA stores.  The
 //               A scales come straight from global memory, three chunks
 //               ahead, into registers (a tile's first ones during the previous
@@ -75,23 +74,14 @@ constexpr int REGS_LOW = 64, REGS_HIGH = 216;
 constexpr uint32_t TMEM_COLS = NBUF * BN;
 constexpr uint32_t A_BYTES = BM * BK;
 constexpr uint32_t B_BYTES = BN * BK;
-// Chunk g of a CTA (counted over its tiles) completes on named barrier
-// 1 + g % kChunkBars once the MMA warp (bar.sync), the operand watcher
-// (bar.arrive after the chunk's operands landed) and the 8 promotion warps
-// (bar.arrive after they consumed chunk g - NBUF, which used the same TMEM
-// buffer; virtual arrivals for the first NBUF chunks) have reached it.
-// With kChunkBars >= max(stages, NBUF) no arrival can run ahead into a later
-// use of the same barrier: the watcher's arrival for chunk g follows the
-// load of chunk g, issued after chunk g - stages completed (so after chunk
-// g - kChunkBars's barrier did); a promotion warp's arrival for chunk g
-// follows the completion of chunk g - NBUF (so of chunk g - kChunkBars).
-constexpr int kChunkBars = 4;
-constexpr int kChunkThreads = 32 * (2 + EPI_WARPS);
-// MMA completion of chunk g: mbarrier done[g % kDone], one commit per chunk.
-// kDone >= max(stages, NBUF) keeps every parity wait on it unambiguous: the
-// next phase of done[g % kDone] (chunk g + kDone) cannot complete before the
-// producer and the promotion warps have waited for chunk g.
-constexpr int kDone = 4;
+// Named barriers 1 .. NBUF: the 8 promotion warps hand TMEM buffer b back
+// to the MMA warp through barrier 1 + b (bar.arrive by them, bar.sync by the
+// whole MMA warp).
+constexpr int kRelThreads = 32 * (1 + EPI_WARPS);
+// Named barrier 1 + NBUF: the operand watcher (warp 2) and the MMA warp meet
+// on it once per chunk (bar.red.or: the watcher reports a failed wait).
+constexpr int kOpsBar = 1 + NBUF;
+constexpr int kOpsThreads = 64;
 // Limit of the promotion warps' wait for a chunk's commit (see run_epilogue):
 // far above the longest settable limit of the other waits.
 constexpr uint64_t kHandoffLimitNs = 3 * kMaxWaitLimitNs;
@@ -111,7 +101,8 @@ struct __align__(1024) Smem {
     uint8_t out[EPI_WARPS][32 * 128];   // per promotion warp: 32 rows x 128 B, 128-byte swizzle
     float sb[kSlots][BN];
     uint64_t full[kStages];
-    uint64_t done[kDone];
+    uint64_t empty[kStages];
+    uint64_t tfull[NBUF];
     uint64_t sfull[kSlots];
     uint64_t sempty[kSlots];
     uint64_t drain;
@@ -126,10 +117,6 @@ constexpr size_t smem_bytes() {
 // At most 196 KB, so that the carve-out leaves 60 KB of L1 (measured faster
 // than the 228 KB carve-out with its 28 KB of L1).
 static_assert(smem_bytes<0>() <= 196 * 1024 && smem_bytes<1>() <= 196 * 1024, "shared memory per CTA");
-static_assert(kDone >= Smem<0>::kStages && kDone >= Smem<1>::kStages && kDone >= NBUF, "done ring too short");
-static_assert(kChunkBars >= Smem<0>::kStages && kChunkBars >= Smem<1>::kStages && kChunkBars >= NBUF,
-              "too few chunk barriers");
-static_assert(1 + kChunkBars <= 15, "named barrier ids");
 
 struct Params {
     const float* sa;
@@ -186,13 +173,6 @@ FP8FG_DEV void tile_origin(int64_t t, int64_t m_tiles, int64_t n_tiles, int m_fa
     }
 }
 
-// K chunks this CTA processes over all its tiles (tiles blockIdx.x,
-// blockIdx.x + gridDim.x, ...); below 2^31 (checked on the host).
-FP8FG_DEV uint32_t cta_chunks(int64_t num_tiles, int64_t kb) {
-    const int64_t b = blockIdx.x;
-    return b < num_tiles ? static_cast<uint32_t>(((num_tiles - 1 - b) / gridDim.x + 1) * kb) : 0u;
-}
-
 // Expert owning row m0: the g with offsets[g] <= m0 < offsets[g+1].
 FP8FG_DEV int expert_of(const int32_t* offsets, int G, int64_t m0) {
     int lo = 0, hi = G;
@@ -237,15 +217,10 @@ FP8FG_DEV void run_producer(Smem<kRowB>& sm, const CUtensorMap* tmap_a, const CU
         const int e = p.offsets ? expert_of(p.offsets, p.G, m0) : 0;
         const uint32_t sc_bytes = static_cast<uint32_t>(min(static_cast<int64_t>(BN), p.N - n0) * 4);
         for (int64_t c = 0; c < kb; ++c) {
-            const uint32_t s = g_ab % ST;
-            if (g_ab >= static_cast<uint32_t>(ST)) {
-                // stage s is free once the MMAs of chunk g_ab - ST have completed
-                const uint32_t d = g_ab - ST;
-                if (!mbar_wait_bounded(smem_u32(&sm.done[d % kDone]), (d / kDone) & 1, abort_flag, p.status,
-                                       p.limit_ns, kErrTimeout)) {
-                    ok = false;
-                    break;
-                }
+            const uint32_t s = g_ab % ST, ph = (g_ab / ST) & 1;
+            if (!mbar_wait_bounded(smem_u32(&sm.empty[s]), ph ^ 1, abort_flag, p.status, p.limit_ns, kErrTimeout)) {
+                ok = false;
+                break;
             }
             const uint32_t fb = smem_u32(&sm.full[s]);
             mbar_arrive_expect_tx(fb, A_BYTES + B_BYTES);
@@ -287,63 +262,74 @@ FP8FG_DEV void run_producer(Smem<kRowB>& sm, const CUtensorMap* tmap_a, const CU
 
 // ------------------------------------------------------- operand watcher ---
 // Whole warp; lane 0 waits.  For every chunk, in the MMA warp's order, wait
-// for the stage's "full" mbarrier (skipped after a failed wait: the abort
-// flag is then raised and the MMA warp stops issuing) and arrive on the
-// chunk's named barrier, on every path, so that the MMA warp never waits
-// for an arrival that does not come.
+// for the stage's "full" mbarrier (skipped after a failed wait) and meet the
+// MMA warp on kOpsBar, passing whether this or an earlier wait failed.  Both
+// warps meet exactly once per chunk on every path, so neither runs ahead.
 template <int kRowB>
-FP8FG_DEV void run_watch(Smem<kRowB>& sm, const Params& p, uint32_t chunks, int lane) {
+FP8FG_DEV void run_watch(Smem<kRowB>& sm, const Params& p, int64_t m_tiles, int64_t n_tiles, int64_t kb, int lane) {
     constexpr int ST = Smem<kRowB>::kStages;
     volatile int* abort_flag = &sm.abort_flag;
+    uint32_t g = 0;
+    const int64_t num_tiles = m_tiles * n_tiles;
     bool ok = true;   // warp-uniform
-    for (uint32_t g = 0; g < chunks; ++g) {
-        const uint32_t s = g % ST, ph = (g / ST) & 1;
-        if (ok) {
-            bool f = true;
-            if (lane == 0)
-                f = mbar_wait_bounded(smem_u32(&sm.full[s]), ph, abort_flag, p.status, p.limit_ns, kErrTimeout);
-            ok = __shfl_sync(0xffffffffu, f, 0) != 0;
+    for (int64_t t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+        for (int64_t c = 0; c < kb; ++c, ++g) {
+            const uint32_t s = g % ST, ph = (g / ST) & 1;
+            if (ok) {
+                bool f = true;
+                if (lane == 0)
+                    f = mbar_wait_bounded(smem_u32(&sm.full[s]), ph, abort_flag, p.status, p.limit_ns, kErrTimeout);
+                ok = __shfl_sync(0xffffffffu, f, 0) != 0;
+            }
+            named_sync_or<kOpsThreads>(kOpsBar, !ok);
         }
-        named_arrive<kChunkThreads>(1 + static_cast<int>(g % kChunkBars));
     }
 }
 
 // ----------------------------------------------------------------- MMA ---
-// Whole warp; lane 0 issues.  For every chunk, aborted or not: bar.sync on
-// the chunk's named barrier (the TMEM buffer handed back, the operands
-// landed), the chunk's MMAs unless the kernel is aborting, and one commit to
-// the chunk's "done" mbarrier (with no MMA behind it after an abort, the
-// commit only tracks the earlier ones).  The promotion warps wait for every
-// chunk's commit, so the lock step holds on every path.  The abort flag is
-// read after the commit, off the MMA issue path, and applies from the next
-// chunk on (an MMA issued on operands of an aborted load reads shared memory
-// in bounds; its result is discarded with the kernel's output).
+// Whole warp; lane 0 issues.  Lock step with the promotion warps: before
+// chunk g (g >= 2) the warp takes the hand-back of chunk g-2 on the named
+// barrier of its buffer, and for every chunk, aborted or not, lane 0 commits
+// the buffer's "full" mbarrier (with no MMA after an abort the commit only
+// tracks the earlier ones).  A promotion warp arrives for chunk g only after
+// that commit, so no arrival can run ahead of the MMA warp's bar.sync, and
+// every bar.sync is matched by the 8 arrivals of a chunk already committed.
+// The chunk's operands are reported by the watcher on kOpsBar.
 template <int kRowB>
-FP8FG_DEV void run_mma(Smem<kRowB>& sm, uint32_t tmem_base, const Params& p, uint32_t chunks, int lane) {
+FP8FG_DEV void run_mma(Smem<kRowB>& sm, uint32_t tmem_base, const Params& p, int64_t m_tiles, int64_t n_tiles,
+                       int64_t kb, int lane) {
     constexpr int ST = Smem<kRowB>::kStages;
-    volatile int* abort_flag = &sm.abort_flag;
+    uint32_t g = 0;
+    const int64_t num_tiles = m_tiles * n_tiles;
     bool ok = true;   // warp-uniform
-    for (uint32_t g = 0; g < chunks; ++g) {
-        const uint32_t s = g % ST;
-        const uint32_t buf = g % NBUF;
-        named_sync<kChunkThreads>(1 + static_cast<int>(g % kChunkBars));
-        if (lane == 0) {
-            if (ok) {
-                tc_fence_after();
-                const uint32_t d_tmem = tmem_base + buf * BN;
-                const uint64_t adesc = smem_desc_sw128(smem_u32(sm.a[s]));
-                const uint64_t bdesc = smem_desc_sw128(smem_u32(sm.b[s]));
+    for (int64_t t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+        for (int64_t c = 0; c < kb; ++c, ++g) {
+            const uint32_t s = g % ST;
+            const uint32_t buf = g % NBUF;
+            if (g >= NBUF) named_sync<kRelThreads>(1 + static_cast<int>(buf));
+            if (named_sync_or<kOpsThreads>(kOpsBar, false)) ok = false;
+            if (lane == 0) {
+                if (ok) {
+                    tc_fence_after();
+                    const uint32_t d_tmem = tmem_base + buf * BN;
+                    const uint64_t adesc = smem_desc_sw128(smem_u32(sm.a[s]));
+                    const uint64_t bdesc = smem_desc_sw128(smem_u32(sm.b[s]));
 #pragma unroll
-                for (int kk = 0; kk < BK / MMA_K; ++kk) {
-                    // advance 32 bytes along K inside the 128-byte swizzle atom
-                    const uint64_t koff = static_cast<uint64_t>((kk * MMA_K) >> 4);
-                    mma_f8f6f4(d_tmem, adesc + koff, bdesc + koff, kIdesc, kk > 0 ? 1u : 0u);
+                    for (int kk = 0; kk < BK / MMA_K; ++kk) {
+                        // advance 32 bytes along K inside the 128-byte swizzle atom
+                        const uint64_t koff = static_cast<uint64_t>((kk * MMA_K) >> 4);
+                        mma_f8f6f4(d_tmem, adesc + koff, bdesc + koff, kIdesc, kk > 0 ? 1u : 0u);
+                    }
+                    mma_commit(smem_u32(&sm.empty[s]));
                 }
+                mma_commit(smem_u32(&sm.tfull[buf]));
             }
-            mma_commit(smem_u32(&sm.done[g % kDone]));
+            __syncwarp();
         }
-        ok = __shfl_sync(0xffffffffu, ok && *abort_flag == 0, 0) != 0;
     }
+    // the last hand-back of each buffer that was used
+    for (uint32_t b = 0; b < NBUF; ++b)
+        if (g > b) named_sync<kRelThreads>(1 + static_cast<int>(b));
     if (lane == 0) {
         // every MMA issued by this thread has finished before TMEM is released
         mma_commit(smem_u32(&sm.drain));
@@ -354,29 +340,18 @@ FP8FG_DEV void run_mma(Smem<kRowB>& sm, uint32_t tmem_base, const Params& p, uin
 
 // ------------------------------------------------------------ promotion ---
 // acc[0..15] += P[0..15] * scale (block B scales) or
-// acc[0..15] += (P[0..15] * sbv[0..15]) * sa (per-row B scales, sbv loaded
-// into registers one 16-column slice ahead).
+// acc[0..15] += (P[0..15] * sbrow[0..15]) * sa (per-row B scales).
 template <int kRowB>
-FP8FG_DEV void promote16(float* acc, const uint32_t (&r)[16], float scale, const float4 (&sbv)[4]) {
+FP8FG_DEV void promote16(float* acc, const uint32_t (&r)[16], float scale, const float* sbrow) {
 #pragma unroll
     for (int k = 0; k < 16; k += 2) {
         float x0 = __uint_as_float(r[k]), x1 = __uint_as_float(r[k + 1]);
         if (kRowB) {
-            const float4 v = sbv[k / 4];
-            if (k % 4 == 0)
-                mul2(x0, x1, v.x, v.y);
-            else
-                mul2(x0, x1, v.z, v.w);
+            const float2 s2 = *reinterpret_cast<const float2*>(sbrow + k);
+            mul2(x0, x1, s2.x, s2.y);
         }
         fma2(acc[k], acc[k + 1], x0, x1, scale, scale);
     }
-}
-
-// Sixteen per-row B scales of this thread's columns: four 16-byte shared
-// loads, the same address for every lane of the warp (a broadcast).
-FP8FG_DEV void load_sb16(float4 (&v)[4], const float* src) {
-#pragma unroll
-    for (int k = 0; k < 4; ++k) v[k] = reinterpret_cast<const float4*>(src)[k];
 }
 
 // A tile's origin and the first scales its promotion needs, loaded one tile
@@ -426,12 +401,9 @@ FP8FG_DEV void run_epilogue(Smem<kRowB>& sm, uint32_t tmem_base, const Params& p
     const uint32_t t_lane = static_cast<uint32_t>(quad * 32) << 16;
     const uint32_t ob = smem_u32(sm.out[warp - 4]);
     const int64_t num_tiles = m_tiles * n_tiles;
-    const uint32_t chunks = cta_chunks(num_tiles, kb);
     uint32_t g = 0;
     bool dead = false;   // after a failed wait: no work, but still one hand-back per chunk
     bool timed_out = false;
-    // both TMEM buffers start free: the hand-backs of the first NBUF chunks
-    for (uint32_t v = 0; v < NBUF && v < chunks; ++v) named_arrive<kChunkThreads>(1 + static_cast<int>(v % kChunkBars));
     TileScales nts = load_tile_scales<kRowB>(blockIdx.x, p, m_tiles, n_tiles, kb, half, row, lane);
     for (int64_t t = blockIdx.x; t < num_tiles; t += gridDim.x) {
         const int64_t m0 = nts.m0, col0 = nts.col0;
@@ -445,7 +417,7 @@ FP8FG_DEV void run_epilogue(Smem<kRowB>& sm, uint32_t tmem_base, const Params& p
 #pragma unroll
         for (int j = 0; j < ECOLS; ++j) acc[j] = 0.0f;
         for (int64_t c = 0; c < kb; ++c, ++g) {
-            const uint32_t buf = g % NBUF;
+            const uint32_t buf = g % NBUF, tph = (g / NBUF) & 1;
             const uint32_t sl = g % SL, sph = (g / SL) & 1;
             if (!kRowB && c > 0 && (c & 31) == 0) {
                 sb_cur = sb_nxt;
@@ -461,8 +433,7 @@ FP8FG_DEV void run_epilogue(Smem<kRowB>& sm, uint32_t tmem_base, const Params& p
             // longest wait the commit can depend on.
             // (After such a wait has failed, which the lock step rules out,
             // the later ones are kept short so the kernel still ends.)
-            bool ok = wait_plain(smem_u32(&sm.done[g % kDone]), (g / kDone) & 1,
-                                 timed_out ? 1000000ull : kHandoffLimitNs);
+            bool ok = wait_plain(smem_u32(&sm.tfull[buf]), tph, timed_out ? 1000000ull : kHandoffLimitNs);
             if (!__all_sync(0xffffffffu, ok)) {
                 if (lane == 0) {
                     atomicCAS(p.status, 0, kErrTimeout);
@@ -484,31 +455,20 @@ FP8FG_DEV void run_epilogue(Smem<kRowB>& sm, uint32_t tmem_base, const Params& p
                 // ECOLS / 16 loads of 16 columns; the next load is in flight
                 // while the previous 16 columns are folded in (16, not 32:
                 // with 32 the registers spilled)
-                // (per-row B scales: the next slice's 16 scales are loaded
-                // before the wait for the next TMEM load, so that no
-                // shared-memory load sits between a TMEM wait and the
-                // arithmetic it feeds)
                 constexpr int NJ = ECOLS / 16;
                 uint32_t r[2][16];
-                float4 sv[4];
-                if (kRowB) load_sb16(sv, sbrow);
                 tmem_ld_32x32b_x16(taddr, r[0]);
                 tmem_ld_wait(r[0]);
 #pragma unroll
                 for (int j = 0; j < NJ; ++j) {
                     if (j + 1 < NJ) tmem_ld_32x32b_x16(taddr + 16 * (j + 1), r[(j + 1) & 1]);
-                    promote16<kRowB>(acc + 16 * j, r[j & 1], scale, sv);
-                    if (j + 1 < NJ) {
-                        if (kRowB) load_sb16(sv, sbrow + 16 * (j + 1));
-                        tmem_ld_wait(r[(j + 1) & 1]);
-                    }
+                    promote16<kRowB>(acc + 16 * j, r[j & 1], scale, sbrow + 16 * j);
+                    if (j + 1 < NJ) tmem_ld_wait(r[(j + 1) & 1]);
                 }
             }
-            // the buffer goes back only after the loaded registers are
-            // consumed: an arrival on the barrier of chunk g + NBUF, the next
-            // user of this buffer
+            // the buffer goes back only after the loaded registers are consumed
             tc_fence_before();
-            if (g + NBUF < chunks) named_arrive<kChunkThreads>(1 + static_cast<int>((g + NBUF) % kChunkBars));
+            named_arrive<kRelThreads>(1 + static_cast<int>(buf));
             if (kRowB && !dead && lane == 0) mbar_arrive(smem_u32(&sm.sempty[sl]));
         }
         if (t + gridDim.x < num_tiles)
@@ -568,8 +528,11 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int64_t m_tiles = p.M / BM, n_tiles = (p.N + BN - 1) / BN, kb = p.K / BK;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < S::kStages; ++s) mbar_init(smem_u32(&sm.full[s]), 1);
-        for (int d = 0; d < kDone; ++d) mbar_init(smem_u32(&sm.done[d]), 1);
+        for (int s = 0; s < S::kStages; ++s) {
+            mbar_init(smem_u32(&sm.full[s]), 1);
+            mbar_init(smem_u32(&sm.empty[s]), 1);
+        }
+        for (int b = 0; b < NBUF; ++b) mbar_init(smem_u32(&sm.tfull[b]), 1);
         for (int s = 0; s < S::kSlots; ++s) {
             mbar_init(smem_u32(&sm.sfull[s]), 1);
             mbar_init(smem_u32(&sm.sempty[s]), EPI_WARPS);
@@ -605,9 +568,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     } else if (warp < 4) {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(REGS_LOW));
         if (warp == 0 && lane == 0) run_producer<kRowB>(sm, &tmap_a, &tmap_b, p, m_tiles, n_tiles, kb);
-        const uint32_t chunks = cta_chunks(m_tiles * n_tiles, kb);
-        if (warp == 1) run_mma<kRowB>(sm, tmem_base, p, chunks, lane);
-        if (warp == 2) run_watch<kRowB>(sm, p, chunks, lane);
+        if (warp == 1) run_mma<kRowB>(sm, tmem_base, p, m_tiles, n_tiles, kb, lane);
+        if (warp == 2) run_watch<kRowB>(sm, p, m_tiles, n_tiles, kb, lane);
     } else {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(REGS_HIGH));
         run_epilogue<kRowB>(sm, tmem_base, p, &tmap_d, m_tiles, n_tiles, kb, warp, lane);
