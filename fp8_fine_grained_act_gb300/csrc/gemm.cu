@@ -26,11 +26,18 @@
 //               warps on a named barrier (bar.sync), learns from warp 2 on
 //               another named barrier that the chunk's operands have landed,
 //               then issues 4 x tcgen05.mma.kind::f8f6f4 (K = 32 each) per
-//               chunk into one of two 256-column buffers and commits to the
-//               stage's "empty" mbarrier and the buffer's "full" one.  The
-//               warp touches no shared memory in this loop: an mbarrier
-//               wait in the MMA-issuing warp measured 150-300 cycles per
-//               chunk even on a completed phase, idling the tensor pipe;
+//               chunk into one of two 256-column buffers and commits ONCE, to
+//               the chunk's "done" mbarrier, on which both the producer
+//               (stage free) and the promotion warps (partial sums ready)
+//               wait.  The warp touches no shared memory in this loop: an
+//               mbarrier wait in the MMA-issuing warp measured 150-300
+//               cycles per chunk even on a completed phase, idling the
+//               tensor pipe.  Its loop is kept to the barrier pair, the
+//               MMAs and one commit: everything it does between a chunk's
+//               last MMA issue and the next chunk's first is time the tensor
+//               pipe can idle (a clock64-traced build measured ~700 cycles
+//               per chunk for this loop with two commits and per-chunk
+//               descriptor arithmetic, against 512 for the MMAs);
 //   warp 2      operand watcher: waits for each chunk's "full" mbarrier and
 //               meets the MMA warp on a named barrier (bar.red.or carries a
 //               failed wait);
@@ -82,6 +89,14 @@ constexpr int kRelThreads = 32 * (1 + EPI_WARPS);
 // on it once per chunk (bar.red.or: the watcher reports a failed wait).
 constexpr int kOpsBar = 1 + NBUF;
 constexpr int kOpsThreads = 64;
+// MMA completion of chunk g (counted over the CTA's tiles): mbarrier
+// done[g % kDone], one commit per chunk.  kDone >= max(stages, NBUF) keeps
+// every parity wait on it unambiguous: the next phase of done[g % kDone]
+// (chunk g + kDone) cannot complete before the producer and the promotion
+// warps have waited for chunk g (the producer has not loaded chunk
+// g + kDone's operands yet, and the MMA warp issues it only after the
+// promotion warps hand back chunk g + kDone - NBUF >= g).
+constexpr uint32_t kDone = 4;
 // Limit of the promotion warps' wait for a chunk's commit (see run_epilogue):
 // far above the longest settable limit of the other waits.
 constexpr uint64_t kHandoffLimitNs = 3 * kMaxWaitLimitNs;
@@ -101,8 +116,7 @@ struct __align__(1024) Smem {
     uint8_t out[EPI_WARPS][32 * 128];   // per promotion warp: 32 rows x 128 B, 128-byte swizzle
     float sb[kSlots][BN];
     uint64_t full[kStages];
-    uint64_t empty[kStages];
-    uint64_t tfull[NBUF];
+    uint64_t done[kDone];
     uint64_t sfull[kSlots];
     uint64_t sempty[kSlots];
     uint64_t drain;
@@ -117,6 +131,8 @@ constexpr size_t smem_bytes() {
 // At most 196 KB, so that the carve-out leaves 60 KB of L1 (measured faster
 // than the 228 KB carve-out with its 28 KB of L1).
 static_assert(smem_bytes<0>() <= 196 * 1024 && smem_bytes<1>() <= 196 * 1024, "shared memory per CTA");
+static_assert(kDone == 4 && kDone >= Smem<0>::kStages && kDone >= Smem<1>::kStages && kDone >= NBUF,
+              "done ring: a power of two no shorter than the stage ring and the TMEM buffers");
 
 struct Params {
     const float* sa;
@@ -217,10 +233,24 @@ FP8FG_DEV void run_producer(Smem<kRowB>& sm, const CUtensorMap* tmap_a, const CU
         const int e = p.offsets ? expert_of(p.offsets, p.G, m0) : 0;
         const uint32_t sc_bytes = static_cast<uint32_t>(min(static_cast<int64_t>(BN), p.N - n0) * 4);
         for (int64_t c = 0; c < kb; ++c) {
-            const uint32_t s = g_ab % ST, ph = (g_ab / ST) & 1;
-            if (!mbar_wait_bounded(smem_u32(&sm.empty[s]), ph ^ 1, abort_flag, p.status, p.limit_ns, kErrTimeout)) {
-                ok = false;
-                break;
+            const uint32_t s = g_ab % ST;
+            if (g_ab >= static_cast<uint32_t>(ST)) {
+                // Stage s is free once the load of chunk d = g_ab - ST into it
+                // has landed and that chunk's MMAs have completed.  The first
+                // wait is needed on the abort path only: a chunk whose
+                // operands the watcher did not confirm is committed without
+                // MMAs, possibly while its load is still in flight, and a
+                // second load into the stage must never be issued on top of
+                // it (each stage has at most one load in flight, so the
+                // tear-down below can wait for every copy to land).
+                const uint32_t d = g_ab - ST;
+                if (!mbar_wait_bounded(smem_u32(&sm.full[s]), (d / ST) & 1, abort_flag, p.status, p.limit_ns,
+                                       kErrTimeout) ||
+                    !mbar_wait_bounded(smem_u32(&sm.done[d % kDone]), (d / kDone) & 1, abort_flag, p.status,
+                                       p.limit_ns, kErrTimeout)) {
+                    ok = false;
+                    break;
+                }
             }
             const uint32_t fb = smem_u32(&sm.full[s]);
             mbar_arrive_expect_tx(fb, A_BYTES + B_BYTES);
@@ -290,46 +320,57 @@ FP8FG_DEV void run_watch(Smem<kRowB>& sm, const Params& p, int64_t m_tiles, int6
 // Whole warp; lane 0 issues.  Lock step with the promotion warps: before
 // chunk g (g >= 2) the warp takes the hand-back of chunk g-2 on the named
 // barrier of its buffer, and for every chunk, aborted or not, lane 0 commits
-// the buffer's "full" mbarrier (with no MMA after an abort the commit only
+// the chunk's "done" mbarrier (with no MMA after an abort the commit only
 // tracks the earlier ones).  A promotion warp arrives for chunk g only after
 // that commit, so no arrival can run ahead of the MMA warp's bar.sync, and
 // every bar.sync is matched by the 8 arrivals of a chunk already committed.
-// The chunk's operands are reported by the watcher on kOpsBar.
+// The chunk's operands are reported by the watcher on kOpsBar, before any
+// MMA of the chunk is issued.  The chunks of all the CTA's tiles form one
+// flat loop with the stage, buffer and descriptors stepped incrementally.
 template <int kRowB>
 FP8FG_DEV void run_mma(Smem<kRowB>& sm, uint32_t tmem_base, const Params& p, int64_t m_tiles, int64_t n_tiles,
                        int64_t kb, int lane) {
     constexpr int ST = Smem<kRowB>::kStages;
-    uint32_t g = 0;
     const int64_t num_tiles = m_tiles * n_tiles;
+    const int64_t b = blockIdx.x;
+    const uint32_t chunks = b < num_tiles ? static_cast<uint32_t>(((num_tiles - 1 - b) / gridDim.x + 1) * kb) : 0u;
+    // descriptors of stage 0; stage s is A_BYTES * s (B_BYTES * s) further,
+    // i.e. (A_BYTES >> 4) * s in the descriptor's start-address field
+    const uint64_t adesc0 = smem_desc_sw128(smem_u32(sm.a[0]));
+    const uint64_t bdesc0 = smem_desc_sw128(smem_u32(sm.b[0]));
+    uint32_t soff_a = 0, soff_b = 0, s = 0, buf = 0;
     bool ok = true;   // warp-uniform
-    for (int64_t t = blockIdx.x; t < num_tiles; t += gridDim.x) {
-        for (int64_t c = 0; c < kb; ++c, ++g) {
-            const uint32_t s = g % ST;
-            const uint32_t buf = g % NBUF;
-            if (g >= NBUF) named_sync<kRelThreads>(1 + static_cast<int>(buf));
-            if (named_sync_or<kOpsThreads>(kOpsBar, false)) ok = false;
-            if (lane == 0) {
-                if (ok) {
-                    tc_fence_after();
-                    const uint32_t d_tmem = tmem_base + buf * BN;
-                    const uint64_t adesc = smem_desc_sw128(smem_u32(sm.a[s]));
-                    const uint64_t bdesc = smem_desc_sw128(smem_u32(sm.b[s]));
+    for (uint32_t g = 0; g < chunks; ++g) {
+        if (g >= NBUF) named_sync<kRelThreads>(1 + static_cast<int>(buf));
+        if (named_sync_or<kOpsThreads>(kOpsBar, false)) ok = false;
+        if (lane == 0) {
+            if (ok) {
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + buf * BN;
+                const uint64_t adesc = adesc0 + soff_a, bdesc = bdesc0 + soff_b;
 #pragma unroll
-                    for (int kk = 0; kk < BK / MMA_K; ++kk) {
-                        // advance 32 bytes along K inside the 128-byte swizzle atom
-                        const uint64_t koff = static_cast<uint64_t>((kk * MMA_K) >> 4);
-                        mma_f8f6f4(d_tmem, adesc + koff, bdesc + koff, kIdesc, kk > 0 ? 1u : 0u);
-                    }
-                    mma_commit(smem_u32(&sm.empty[s]));
+                for (int kk = 0; kk < BK / MMA_K; ++kk) {
+                    // advance 32 bytes along K inside the 128-byte swizzle atom
+                    const uint64_t koff = static_cast<uint64_t>((kk * MMA_K) >> 4);
+                    mma_f8f6f4(d_tmem, adesc + koff, bdesc + koff, kIdesc, kk > 0 ? 1u : 0u);
                 }
-                mma_commit(smem_u32(&sm.tfull[buf]));
             }
-            __syncwarp();
+            mma_commit(smem_u32(&sm.done[g & (kDone - 1)]));
+        }
+        __syncwarp();
+        buf ^= 1u;
+        if (++s == static_cast<uint32_t>(ST)) {
+            s = 0;
+            soff_a = 0;
+            soff_b = 0;
+        } else {
+            soff_a += A_BYTES >> 4;
+            soff_b += B_BYTES >> 4;
         }
     }
     // the last hand-back of each buffer that was used
-    for (uint32_t b = 0; b < NBUF; ++b)
-        if (g > b) named_sync<kRelThreads>(1 + static_cast<int>(b));
+    for (uint32_t bb = 0; bb < NBUF; ++bb)
+        if (chunks > bb) named_sync<kRelThreads>(1 + static_cast<int>(bb));
     if (lane == 0) {
         // every MMA issued by this thread has finished before TMEM is released
         mma_commit(smem_u32(&sm.drain));
@@ -340,18 +381,29 @@ FP8FG_DEV void run_mma(Smem<kRowB>& sm, uint32_t tmem_base, const Params& p, int
 
 // ------------------------------------------------------------ promotion ---
 // acc[0..15] += P[0..15] * scale (block B scales) or
-// acc[0..15] += (P[0..15] * sbrow[0..15]) * sa (per-row B scales).
+// acc[0..15] += (P[0..15] * sbv[0..15]) * sa (per-row B scales, sbv loaded
+// into registers before the wait for the TMEM load they are used with).
 template <int kRowB>
-FP8FG_DEV void promote16(float* acc, const uint32_t (&r)[16], float scale, const float* sbrow) {
+FP8FG_DEV void promote16(float* acc, const uint32_t (&r)[16], float scale, const float4 (&sbv)[4]) {
 #pragma unroll
     for (int k = 0; k < 16; k += 2) {
         float x0 = __uint_as_float(r[k]), x1 = __uint_as_float(r[k + 1]);
         if (kRowB) {
-            const float2 s2 = *reinterpret_cast<const float2*>(sbrow + k);
-            mul2(x0, x1, s2.x, s2.y);
+            const float4 v = sbv[k / 4];
+            if (k % 4 == 0)
+                mul2(x0, x1, v.x, v.y);
+            else
+                mul2(x0, x1, v.z, v.w);
         }
         fma2(acc[k], acc[k + 1], x0, x1, scale, scale);
     }
+}
+
+// Sixteen per-row B scales of this thread's columns: four 16-byte shared
+// loads, the same address for every lane of the warp (a broadcast).
+FP8FG_DEV void load_sb16(float4 (&v)[4], const float* src) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) v[k] = reinterpret_cast<const float4*>(src)[k];
 }
 
 // A tile's origin and the first scales its promotion needs, loaded one tile
@@ -363,7 +415,7 @@ struct TileScales {
     const float* sbp;       // block B scales of this warp's 128 columns, chunk 0
     const float* sap;       // A scale of this thread's row, chunk 0
     float sb_cur, sb_nxt;   // block B scales: lane l holds chunk l / 32 + l
-    float q0, q1, q2;       // A scales of chunks 0, 1, 2
+    float q[4];             // A scales of chunks 0 .. 3 (a chunk past the tile's last repeats the last)
 };
 
 template <int kRowB>
@@ -384,9 +436,10 @@ FP8FG_DEV TileScales load_tile_scales(int64_t t, const Params& p, int64_t m_tile
         if (ts.active && lane + 32 < kb) ts.sb_nxt = __ldg(ts.sbp + (lane + 32) * p.sb_stride_k);
     }
     ts.sap = p.sa + ts.m0 + row;
-    ts.q0 = __ldg(ts.sap);
-    ts.q1 = kb > 1 ? __ldg(ts.sap + p.M) : 0.0f;
-    ts.q2 = kb > 2 ? __ldg(ts.sap + 2 * p.M) : 0.0f;
+    // (indices clamped to the last chunk instead of a select on the loaded
+    // value: a select would make the thread wait for the load to return)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) ts.q[j] = __ldg(ts.sap + min(static_cast<int64_t>(j), kb - 1) * p.M);
     return ts;
 }
 
@@ -411,29 +464,34 @@ FP8FG_DEV void run_epilogue(Smem<kRowB>& sm, uint32_t tmem_base, const Params& p
         const float* sbp = nts.sbp;
         const float* sap = nts.sap;
         float sb_cur = nts.sb_cur, sb_nxt = nts.sb_nxt;
-        // A scales of chunks c, c+1, c+2 in flight
-        float q0 = nts.q0, q1 = nts.q1, q2 = nts.q2;
+        // A scales of four consecutive chunks in a register ring: the chunk
+        // loop below is unrolled by four and each copy of its body names its
+        // own ring register, so the scale of chunk c + 4, loaded while chunk
+        // c is promoted, is first read four chunks later (a rotation of the
+        // registers would read the newest load at once and wait for it)
+        float qa0 = nts.q[0], qa1 = nts.q[1], qa2 = nts.q[2], qa3 = nts.q[3];
         float acc[ECOLS];
 #pragma unroll
         for (int j = 0; j < ECOLS; ++j) acc[j] = 0.0f;
-        for (int64_t c = 0; c < kb; ++c, ++g) {
-            const uint32_t buf = g % NBUF, tph = (g / NBUF) & 1;
+        auto chunk = [&](int64_t c, float& qa) {
+            const uint32_t buf = g % NBUF;
             const uint32_t sl = g % SL, sph = (g / SL) & 1;
             if (!kRowB && c > 0 && (c & 31) == 0) {
                 sb_cur = sb_nxt;
-                sb_nxt = (active && c + 32 + lane < kb) ? __ldg(sbp + (c + 32 + lane) * p.sb_stride_k) : 0.0f;
+                if (active) sb_nxt = __ldg(sbp + min(c + 32 + lane, kb - 1) * p.sb_stride_k);
             }
-            const float sa_i = q0;
-            q0 = q1;
-            q1 = q2;
-            q2 = c + 3 < kb ? __ldg(sap + (c + 3) * p.M) : 0.0f;
+            const float sa_i = qa;
+            // chunk c + 4's scale; past the tile's last chunk the (unused)
+            // load repeats the last one: an unconditional load
+            qa = __ldg(sap + min(c + 4, kb - 1) * p.M);
             // Every lane waits (each gets the barrier's acquire).  The MMA
             // warp commits this barrier for every chunk, aborted or not, so
             // the wait ignores the abort flag; its limit is far above the
             // longest wait the commit can depend on.
             // (After such a wait has failed, which the lock step rules out,
             // the later ones are kept short so the kernel still ends.)
-            bool ok = wait_plain(smem_u32(&sm.tfull[buf]), tph, timed_out ? 1000000ull : kHandoffLimitNs);
+            bool ok = wait_plain(smem_u32(&sm.done[g & (kDone - 1)]), (g / kDone) & 1,
+                                 timed_out ? 1000000ull : kHandoffLimitNs);
             if (!__all_sync(0xffffffffu, ok)) {
                 if (lane == 0) {
                     atomicCAS(p.status, 0, kErrTimeout);
@@ -454,22 +512,37 @@ FP8FG_DEV void run_epilogue(Smem<kRowB>& sm, uint32_t tmem_base, const Params& p
                 const float* sbrow = sm.sb[sl] + ECOLS * half;
                 // ECOLS / 16 loads of 16 columns; the next load is in flight
                 // while the previous 16 columns are folded in (16, not 32:
-                // with 32 the registers spilled)
+                // with 32 the registers spilled).  Per-row B scales: the next
+                // slice's 16 scales are loaded before the wait for the next
+                // TMEM load, so that no shared-memory load sits between a
+                // TMEM wait and the arithmetic it feeds.
                 constexpr int NJ = ECOLS / 16;
                 uint32_t r[2][16];
+                float4 sv[4];
+                if (kRowB) load_sb16(sv, sbrow);
                 tmem_ld_32x32b_x16(taddr, r[0]);
                 tmem_ld_wait(r[0]);
 #pragma unroll
                 for (int j = 0; j < NJ; ++j) {
                     if (j + 1 < NJ) tmem_ld_32x32b_x16(taddr + 16 * (j + 1), r[(j + 1) & 1]);
-                    promote16<kRowB>(acc + 16 * j, r[j & 1], scale, sbrow + 16 * j);
-                    if (j + 1 < NJ) tmem_ld_wait(r[(j + 1) & 1]);
+                    promote16<kRowB>(acc + 16 * j, r[j & 1], scale, sv);
+                    if (j + 1 < NJ) {
+                        if (kRowB) load_sb16(sv, sbrow + 16 * (j + 1));
+                        tmem_ld_wait(r[(j + 1) & 1]);
+                    }
                 }
             }
             // the buffer goes back only after the loaded registers are consumed
             tc_fence_before();
             named_arrive<kRelThreads>(1 + static_cast<int>(buf));
             if (kRowB && !dead && lane == 0) mbar_arrive(smem_u32(&sm.sempty[sl]));
+            ++g;
+        };
+        for (int64_t c = 0; c < kb; c += 4) {
+            chunk(c, qa0);
+            if (c + 1 < kb) chunk(c + 1, qa1);
+            if (c + 2 < kb) chunk(c + 2, qa2);
+            if (c + 3 < kb) chunk(c + 3, qa3);
         }
         if (t + gridDim.x < num_tiles)
             nts = load_tile_scales<kRowB>(t + gridDim.x, p, m_tiles, n_tiles, kb, half, row, lane);
@@ -528,11 +601,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int64_t m_tiles = p.M / BM, n_tiles = (p.N + BN - 1) / BN, kb = p.K / BK;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < S::kStages; ++s) {
-            mbar_init(smem_u32(&sm.full[s]), 1);
-            mbar_init(smem_u32(&sm.empty[s]), 1);
-        }
-        for (int b = 0; b < NBUF; ++b) mbar_init(smem_u32(&sm.tfull[b]), 1);
+        for (int s = 0; s < S::kStages; ++s) mbar_init(smem_u32(&sm.full[s]), 1);
+        for (uint32_t d = 0; d < kDone; ++d) mbar_init(smem_u32(&sm.done[d]), 1);
         for (int s = 0; s < S::kSlots; ++s) {
             mbar_init(smem_u32(&sm.sfull[s]), 1);
             mbar_init(smem_u32(&sm.sempty[s]), EPI_WARPS);
