@@ -720,6 +720,20 @@ def run_gpu(args):
     e2e_ms = max_over_ranks(p0.elapsed_time(p1) / e2e_steps)
     del xs[1], ws[1], ys[1], yhs[1]
 
+    # the activation quantizer fused into the GEMM (one launch): the same
+    # step with fp8_gemm_quant_a in place of the 1x128 quantizer + GEMM
+    flags = torch.empty((M // 128,), dtype=torch.int32, device=dev)
+    fused_k = [("w", lambda i: fb.fp8_quant_w_128x128(w, q=qw, scales=sw, stream=stream)),
+               ("fused", lambda i: fb.fp8_gemm_quant_a(x, qw, sw, out_dtype=fb.FP8FG_OUT_BF16, q_a=qx, s_a=sx,
+                                                       d=y, band_flags=flags, stream=stream))]
+    f_rounds = block_rounds(fused_k, stream, min(args.block_seconds, 1.0), 3)
+    with ClockSampler(local) as clk_f:
+        f_per, _ = timed_rounds(fused_k, f_rounds, stream)
+    if fb.fp8fg_last_device_status() != 0:
+        raise SystemExit("fused step: device status not clean")
+    t_fused = max_over_ranks(f_per[1])
+    t_fused_step = max_over_ranks(sum(f_per))
+
     ms_step = max_over_ranks(total_ms / args.steps)
     t_gemm = max_over_ranks(t_gemm)
     t_act = max_over_ranks(t_act)
@@ -732,6 +746,10 @@ def run_gpu(args):
                          "gemm_blockscaled fprop 4096x18432x7168 bf16": pk.gemm(FLOPS, t_gemm),
                          "step": {"ms": ms_step, "soak_ms_per_step": soak_ms, "soak_steps": soak_steps,
                                   "l2": "inputs larger than L2: each step reads X (58.7 MB) and W (528 MB)"},
+                         "gemm_quant_a (1x128 quantizer fused into the GEMM, one launch)": pk.gemm(
+                             FLOPS, t_fused, {"two_launches_us": (t_act + t_gemm) * 1e3,
+                                              "step_with_fused_ms": t_fused_step, "rounds": f_rounds,
+                                              "clocks": clk_f.summary()}),
                          "clocks": clk.summary()}}
     launches = 3 * args.steps
     if single:

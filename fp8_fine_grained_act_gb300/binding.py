@@ -44,6 +44,7 @@ SIGNATURES = {
     "fp8_quant_act_dual": (_i32, [_vp, _i64, _i64, _vp, _vp, _vp, _vp, _vp]),
     "fp8_gemm_blockscaled": (_i32, [_vp, _vp, _vp, _vp, _i32, _i64, _i64, _vp, _i32, _i64, _i64, _i64, _vp]),
     "fp8_gemm_grouped": (_i32, [_vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i64, _i64, _i64, _vp]),
+    "fp8_gemm_quant_a": (_i32, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _vp, _i32, _i64, _i64, _i64, _vp, _vp]),
     "fp8fg_status_string": (ctypes.c_char_p, [_i32]),
     "fp8fg_last_device_status": (_i32, [_vp]),
     "fp8fg_selftest_watchdog": (_i32, [_i64, _vp]),
@@ -233,6 +234,45 @@ def fp8_gemm_blockscaled(a, sa, b, sb, bscale: int = FP8FG_BSCALE_BLOCK128, sb_s
                                      _ptr(d), int(out_dtype), M, N, K, _stream(stream))
     _check(st, "fp8_gemm_blockscaled")
     return d
+
+
+def fp8_gemm_quant_a(x, b, sb, sb_strides=None, out_dtype: int = FP8FG_OUT_BF16, q_a=None, s_a=None, d=None,
+                     band_flags=None, stream=None):
+    """The 1x128 quantizer fused into the block-scaled GEMM (one launch):
+    BF16 x[M, K], B codes b[N, K] with 128x128 block scales sb ->
+    (d[M, N], q_a[M, K], s_a[K/128, M]); q_a and s_a are what
+    fp8_quant_act_1x128(x) returns.  band_flags: int32[M/128] device
+    workspace (allocated when not given)."""
+    if not isinstance(x, torch.Tensor) or x.dim() != 2 or not isinstance(b, torch.Tensor) or b.dim() != 2:
+        raise ValueError("x must be [M, K] and b [N, K]")
+    M, K = x.shape
+    N = b.shape[0]
+    if b.shape[1] != K:
+        raise ValueError("x and b disagree on K")
+    dev = x.device
+    _need(x, torch.bfloat16, (M, K), "x", dev)
+    _need(b, torch.uint8, (N, K), "b", dev)
+    sn, sk = sb_strides if sb_strides is not None else (K // GROUP, 1)
+    if sn < 0 or sk < 0:
+        raise ValueError("sb_strides must be non-negative")
+    last = (max(N // GROUP - 1, 0) * sn + max(K // GROUP - 1, 0) * sk + 1) if N and K else 0
+    _need_flat(sb, torch.float32, last, "sb", dev)
+    if q_a is None:
+        q_a = torch.empty((M, K), dtype=torch.uint8, device=dev)
+    if s_a is None:
+        s_a = torch.empty((K // GROUP, M), dtype=torch.float32, device=dev)
+    if band_flags is None:
+        band_flags = torch.empty((max(M // GROUP, 1),), dtype=torch.int32, device=dev)
+    _need(q_a, torch.uint8, (M, K), "q_a", dev)
+    _need(s_a, torch.float32, (K // GROUP, M), "s_a", dev)
+    if band_flags.dtype != torch.int32 or not band_flags.is_cuda or band_flags.numel() < M // GROUP \
+            or not band_flags.is_contiguous() or band_flags.device != dev:
+        raise ValueError(f"band_flags: a contiguous CUDA int32 tensor of >= {M // GROUP} elements on {dev}")
+    d = _out(d, M, N, out_dtype, dev)
+    st = load().fp8_gemm_quant_a(_ptr(x), _ptr(q_a), _ptr(s_a), _ptr(b), _ptr(sb), int(sn), int(sk), _ptr(d),
+                                 int(out_dtype), M, N, K, _ptr(band_flags), _stream(stream))
+    _check(st, "fp8_gemm_quant_a")
+    return d, q_a, s_a
 
 
 def fp8_gemm_grouped(a, sa, b, sb, group_offsets, out_dtype: int = FP8FG_OUT_BF16, d=None, stream=None):

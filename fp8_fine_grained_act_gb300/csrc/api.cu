@@ -184,6 +184,52 @@ int fp8_gemm_blockscaled(const uint8_t* a, const float* sa, const uint8_t* b, co
     return gemm_common(g, stream);
 }
 
+int fp8_gemm_quant_a(const void* a_bf16, uint8_t* q_a, float* s_a, const uint8_t* b, const float* sb,
+                     int64_t sb_stride_n, int64_t sb_stride_k, void* d, int out_dtype, int64_t M, int64_t N,
+                     int64_t K, int32_t* band_flags, cudaStream_t stream) {
+    int st = check_gemm_shape(M, N, K, out_dtype);
+    if (st != kOk) return st;
+    if (sb_stride_n < 0 || sb_stride_k < 0) return kErrInvalidArg;
+    if (M == 0) return kOk;
+    // with K == 0 there is nothing to read or quantize: only d is touched
+    if ((K > 0 && (!a_bf16 || !q_a || !s_a || !band_flags)) || (N > 0 && (!d || (K > 0 && (!b || !sb)))))
+        return kErrInvalidArg;
+    if (M > (int64_t(1) << 40) / (K > 0 ? K : 1)) return kErrInvalidArg;
+    if ((K > 0 && (!aligned16(a_bf16) || !aligned16(q_a) || !aligned4(s_a) || !aligned4(band_flags))) ||
+        (N > 0 && (!aligned16(d) || (K > 0 && (!aligned16(b) || !aligned4(sb))))))
+        return kErrMisaligned;
+    DeviceInfo* dv = nullptr;
+    st = current_device(&dv);
+    if (st != kOk) return st;
+    if (K == 0) {
+        // no groups to quantize; D = 0
+        if (N == 0) return kOk;
+        const size_t elt = out_dtype == FP8FG_OUT_BF16 ? 2 : 4;
+        return from_cuda(cudaMemsetAsync(d, 0, static_cast<size_t>(M) * N * elt, stream));
+    }
+    // the 1x128 quantizer's grid limits (a GEMM with no columns is that quantizer alone)
+    if (K / 128 > 65535 || M / 64 >= (int64_t(1) << 31)) return kErrInvalidArg;
+    if (N == 0) return from_cuda(launch_quant_act_rows(a_bf16, M, K, q_a, s_a, dv->num_sms, stream));
+    GemmArgs g{};
+    g.a = q_a;
+    g.sa = s_a;
+    g.b = b;
+    g.sb = sb;
+    g.bscale = FP8FG_BSCALE_BLOCK128;
+    g.sb_stride_n = sb_stride_n;
+    g.sb_stride_k = sb_stride_k;
+    g.d = d;
+    g.out_bf16 = out_dtype == FP8FG_OUT_BF16;
+    g.M = M;
+    g.N = N;
+    g.K = K;
+    g.offsets = nullptr;
+    g.G = 0;
+    g.xa = a_bf16;
+    g.band_flags = band_flags;
+    return gemm_common(g, stream);
+}
+
 int fp8_gemm_grouped(const uint8_t* a, const float* sa, const uint8_t* b, const float* sb,
                      const int32_t* group_offsets, int G, void* d, int out_dtype, int64_t M_total, int64_t N,
                      int64_t K, cudaStream_t stream) {

@@ -62,6 +62,7 @@
 
 #include "kernels.h"
 #include "ptx.cuh"
+#include "quant_math.cuh"
 
 namespace fp8fg {
 namespace {
@@ -120,6 +121,8 @@ struct __align__(1024) Smem {
     uint64_t sfull[kSlots];
     uint64_t sempty[kSlots];
     uint64_t drain;
+    uint64_t pfull[5];    // fused A quantization: tile slot loaded (TMA)
+    uint64_t pempty[5];   // fused A quantization: tile slot consumed (8 warps)
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -149,6 +152,12 @@ struct Params {
     int m_fastest;
     int* status;
     uint64_t limit_ns;
+    // fused A quantization (fp8_gemm_quant_a): the BF16 A operand, the
+    // buffers its codes and scales are written to (the A tensor map and sa
+    // read the same ones), and the per-band tile counters
+    uint2* qa;
+    float* sa_out;
+    int* band_flags;
 };
 
 // Shared-memory matrix descriptor of a K-major tile written by TMA with the
@@ -590,10 +599,150 @@ FP8FG_DEV void run_epilogue(Smem<kRowB>& sm, uint32_t tmem_base, const Params& p
     __syncwarp();
 }
 
+// ------------------------------------------------ fused A quantization ---
+// Phase 1 of fp8_gemm_quant_a: this CTA's share of the 1x128 quantization of
+// the BF16 A operand into q_a / s_a, the buffers the GEMM phase then reads
+// (the codes through the A tensor map).  Work: 128-row x 128-column tiles in
+// band-major order (tile t: 128-row band t / kb, group column t % kb), tile t
+// done by CTA t % gridDim.x.  Thread 0 streams the CTA's tiles with TMA (two
+// 128-row x 64-column boxes per tile, 128-byte swizzle) into a ring of five
+// 32 KB slots laid over the GEMM's idle operand stages and output staging; the 256 threads of
+// warps 4-11 quantize each tile from shared memory with
+// fp8_quant_act_1x128's mapping and arithmetic (a lane quad per row group,
+// lane j holding chunks j, j+4, j+8, j+12; two rows per thread), so the codes
+// and scales are the ones that quantizer writes; once the CTA's share is
+// done, each of its tiles is added to its band's counter with a release at
+// GPU scope.  Sources: DeepSeek-V3 FP8 post
+// (innerforce.co.kr), fine-grained quantization paragraph (1x128 tiles,
+// max-abs scaling, online) and low-precision storage paragraph (activations
+// kept in FP8).
+constexpr int kPhase1Bar = 4;          // named barrier of the 256 phase-1 threads
+constexpr int kPhase1Threads = 256;
+constexpr int kP1Slots = 5;
+constexpr uint32_t kP1SlotBytes = 128 * 128 * 2;   // one BF16 tile: two 16 KB boxes
+constexpr uint32_t kP1BoxBytes = kP1SlotBytes / 2;
+
 template <int kRowB>
+FP8FG_DEV uint32_t p1_slot(Smem<kRowB>& sm, uint32_t i) {
+    static_assert(sizeof(sm.a) + sizeof(sm.b) + sizeof(sm.out) >= kP1Slots * kP1SlotBytes,
+                  "phase-1 ring inside the operand stages and the output staging buffers");
+    return smem_u32(&sm.a[0][0]) + (i % kP1Slots) * kP1SlotBytes;
+}
+
+// Thread 0: load the CTA's tiles into the ring.  Returns the number of tiles
+// whose loads were issued (all of them unless a wait ran out).
+template <int kRowB>
+FP8FG_DEV uint32_t p1_load(Smem<kRowB>& sm, const CUtensorMap* tmap_x, const Params& p, int64_t units, int64_t kb) {
+    volatile int* abort_flag = &sm.abort_flag;
+    uint32_t i = 0;
+    for (int64_t t = blockIdx.x; t < units; t += gridDim.x, ++i) {
+        if (i >= kP1Slots) {
+            const uint32_t prev = i - kP1Slots;   // the tile that used this slot
+            if (!mbar_wait_bounded(smem_u32(&sm.pempty[prev % kP1Slots]), (prev / kP1Slots) & 1, abort_flag,
+                                   p.status, p.limit_ns, kErrTimeout))
+                break;
+        }
+        const uint32_t m = static_cast<uint32_t>(t) / static_cast<uint32_t>(kb);
+        const uint32_t c = static_cast<uint32_t>(t) - m * static_cast<uint32_t>(kb);
+        const uint32_t fb = smem_u32(&sm.pfull[i % kP1Slots]), dst = p1_slot(sm, i);
+        mbar_arrive_expect_tx(fb, kP1SlotBytes);
+        tma_load_2d(dst, tmap_x, static_cast<int32_t>(c * BK), static_cast<int32_t>(m * BM), fb);
+        tma_load_2d(dst + kP1BoxBytes, tmap_x, static_cast<int32_t>(c * BK + 64), static_cast<int32_t>(m * BM), fb);
+    }
+    return i;
+}
+
+// Warps 4-11: quantize the CTA's tiles from the ring.  Returns false after a
+// failed wait (the kernel then computes nothing).
+template <int kRowB>
+FP8FG_DEV bool p1_quantize(Smem<kRowB>& sm, const Params& p, int64_t units, int64_t kb, int tid) {
+    volatile int* abort_flag = &sm.abort_flag;
+    const int j = tid & 3;     // chunks j, j+4, j+8, j+12 of the row group
+    const int rq = tid >> 2;   // row within a 64-row half of the tile
+    const int lane = tid & 31;
+    bool ok = true;            // warp-uniform
+    uint32_t i = 0;
+    for (int64_t t = blockIdx.x; t < units; t += gridDim.x, ++i) {
+        if (ok) {
+            bool f = mbar_wait_bounded(smem_u32(&sm.pfull[i % kP1Slots]), (i / kP1Slots) & 1, abort_flag, p.status,
+                                       p.limit_ns, kErrTimeout);
+            ok = __all_sync(0xffffffffu, f);
+        }
+        if (ok) {
+            // 32-bit index arithmetic: the tile count is below 2^31 (checked on the host)
+            const uint32_t m = static_cast<uint32_t>(t) / static_cast<uint32_t>(kb);
+            const uint32_t c = static_cast<uint32_t>(t) - m * static_cast<uint32_t>(kb);
+            const uint32_t slot = p1_slot(sm, i);
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int r = rq + 64 * u;
+                uint4 v[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    // chunk j + 4k of the row: box k / 2, 16-byte unit j + 4 (k & 1), 128-byte swizzle
+                    const uint32_t unit = static_cast<uint32_t>(j + 4 * (k & 1)) ^ static_cast<uint32_t>(r & 7);
+                    v[k] = ld_shared_v4(slot + (k >> 1) * kP1BoxBytes + r * 128 + (unit << 4));
+                }
+                const float amax = quad_amax_bf16(v);
+                const float s = __fdiv_rn(amax, 448.0f);
+                const GroupScale gs(s);
+                const int64_t row = static_cast<int64_t>(m) * BM + r;
+                uint2* dst = p.qa + (row * p.K + static_cast<int64_t>(c) * BK) / 8 + j;
+                with_mode(gs, [&](auto md) {
+                    constexpr int kM = decltype(md)::value;
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        uint2 out;
+                        out.x = quant_quad_bf16<kM>(v[k].x, v[k].y, gs);
+                        out.y = quant_quad_bf16<kM>(v[k].z, v[k].w, gs);
+                        __stcs(dst + 4 * k, out);
+                    }
+                });
+                if (j == 0) p.sa_out[static_cast<int64_t>(c) * p.M + row] = s;
+            }
+        }
+        // the slot goes back to the loader (its reads are ordered before the
+        // next TMA write by the mbarrier, as in any TMA consumer ring)
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&sm.pempty[i % kP1Slots]));
+    }
+    // Publish the CTA's tiles once, at the end (fences per tile measured a
+    // store round trip each): this thread's shared reads before the GEMM's
+    // TMA rewrites the stages and its global writes before later TMA reads
+    // of them; the 256 threads' writes; then one GPU-scope fence and a
+    // relaxed add per tile to its band's counter.
+    fence_proxy_async_shared();
+    fence_proxy_async_global();
+    named_sync<kPhase1Threads>(kPhase1Bar);
+    if (tid == 0 && ok) {
+        __threadfence();
+        for (int64_t t = blockIdx.x; t < units; t += gridDim.x) atomicAdd(p.band_flags + t / kb, 1);
+    }
+    return ok;
+}
+
+// Thread 0 of every CTA: wait until every band's kb tiles are published
+// (acquire), bounded by the wait limit; a timeout records
+// FP8FG_ERR_TIMEOUT and the CTA computes nothing.
+FP8FG_DEV bool wait_bands(const Params& p, int64_t m_tiles, int64_t kb) {
+    const uint64_t t0 = globaltimer_ns();
+    for (int64_t m = 0; m < m_tiles; ++m) {
+        while (ld_acquire_gpu(p.band_flags + m) < kb) {
+            if (globaltimer_ns() - t0 > p.limit_ns) {
+                atomicCAS(p.status, 0, kErrTimeout);
+                return false;
+            }
+        }
+    }
+    fence_proxy_async_global();   // before this thread (the producer) issues TMA reads of q_a
+    return true;
+}
+
+template <int kRowB, bool kFusedA>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_blockscaled_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
-                            const __grid_constant__ CUtensorMap tmap_d, const Params p) {
+                            const __grid_constant__ CUtensorMap tmap_d, const __grid_constant__ CUtensorMap tmap_x,
+                            const Params p) {
     using S = Smem<kRowB>;
     extern __shared__ uint8_t smem_raw[];
     S& sm = *reinterpret_cast<S*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -608,9 +757,15 @@ __global__ void __launch_bounds__(THREADS, 1)
             mbar_init(smem_u32(&sm.sempty[s]), EPI_WARPS);
         }
         mbar_init(smem_u32(&sm.drain), 1);
+        for (int s = 0; s < kP1Slots; ++s) {
+            mbar_init(smem_u32(&sm.pfull[s]), 1);
+            mbar_init(smem_u32(&sm.pempty[s]), EPI_WARPS);
+        }
         sm.abort_flag = 0;
         fence_barrier_init();
     }
+    if (kFusedA && threadIdx.x == 0) prefetch_tensormap(&tmap_x);
+    if (kFusedA) __syncthreads();   // the ring's barriers are initialised before phase 1 uses them
     if (warp == 0 && lane == 0) {
         prefetch_tensormap(&tmap_a);
         prefetch_tensormap(&tmap_b);
@@ -629,12 +784,36 @@ __global__ void __launch_bounds__(THREADS, 1)
             if (g > 0 && static_cast<int64_t>(__ldg(p.offsets + g - 1)) > o) bad = 1;
         }
     }
+    int stop = 0;
+    if (kFusedA) {
+        // phase 1 (all CTAs are resident: cooperative launch): quantize this
+        // CTA's share of A, then wait for every CTA's share
+        const int64_t units = m_tiles * kb;
+        if (threadIdx.x == 0) {
+            const uint32_t issued = p1_load(sm, &tmap_x, p, units, kb);
+            if (!wait_bands(p, m_tiles, kb)) stop = 1;
+            if (stop || *static_cast<volatile int*>(&sm.abort_flag)) {
+                // let every copy issued into the ring land before the stages are reused or released
+                bool landed = true;
+                for (uint32_t s = 0; s < kP1Slots && s < issued; ++s) {
+                    const uint32_t last = s + kP1Slots * ((issued - 1 - s) / kP1Slots);
+                    landed &= wait_plain(smem_u32(&sm.pfull[s]), (last / kP1Slots) & 1, kTeardownLimitNs);
+                }
+                if (!landed) atomicExch(p.status, kErrTeardown);
+                stop = 1;
+            }
+        }
+        if (warp >= 4 && !p1_quantize(sm, p, units, kb, static_cast<int>(threadIdx.x) - 128)) stop = 1;
+    }
     tc_fence_before();
     bad = __syncthreads_or(bad);
+    if (kFusedA) stop = __syncthreads_or(stop);
     tc_fence_after();
     const uint32_t tmem_base = sm.tmem_base;
     if (bad) {
         if (blockIdx.x == 0 && threadIdx.x == 0) atomicCAS(p.status, 0, kErrInvalidArg);
+    } else if (stop) {
+        // a CTA's share of A never arrived: nothing is computed
     } else if (warp < 4) {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(REGS_LOW));
         if (warp == 0 && lane == 0) run_producer<kRowB>(sm, &tmap_a, &tmap_b, p, m_tiles, n_tiles, kb);
@@ -685,6 +864,21 @@ bool encode_operand_map(CUtensorMap* map, const void* base, int64_t rows, int64_
 
 // Output map over D [M, N] (BF16 or FP32): box of 128 bytes of a row x 32
 // rows, 128-byte swizzle (the promotion warps' staging layout).
+// Map over a BF16 activation x[M, K] for the fused A quantization: box of
+// 64 columns (128 bytes) x 128 rows, 128-byte swizzle.
+bool encode_act_map(CUtensorMap* map, const void* base, int64_t M, int64_t K) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = get_encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
+    cuuint32_t box[2] = {64, 128};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 bool encode_output_map(CUtensorMap* map, void* base, int64_t M, int64_t N, bool bf16) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = get_encode_fn();
     if (!enc) return false;
@@ -710,21 +904,27 @@ int launch_gemm(const GemmArgs& a, int num_sms, int* status_word, cudaStream_t s
     if (dev >= 0 && dev < 64) {
         cudaError_t e = cudaSuccess;
         std::call_once(g_attr_once[dev], [&] {
-            e = cudaFuncSetAttribute(gemm_blockscaled_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            e = cudaFuncSetAttribute(gemm_blockscaled_kernel<0, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      static_cast<int>(smem_bytes<0>()));
             if (e == cudaSuccess)
-                e = cudaFuncSetAttribute(gemm_blockscaled_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                e = cudaFuncSetAttribute(gemm_blockscaled_kernel<1, false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem_bytes<1>()));
+            if (e == cudaSuccess)
+                e = cudaFuncSetAttribute(gemm_blockscaled_kernel<0, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem_bytes<0>()));
         });
         if (e != cudaSuccess) {
             *cuda_err = e;
             return kErrCuda;
         }
     }
-    CUtensorMap tmap_a, tmap_b, tmap_d;
+    CUtensorMap tmap_a, tmap_b, tmap_d, tmap_x;
     std::memset(&tmap_a, 0, sizeof tmap_a);
     std::memset(&tmap_b, 0, sizeof tmap_b);
     std::memset(&tmap_d, 0, sizeof tmap_d);
+    std::memset(&tmap_x, 0, sizeof tmap_x);
+    if (a.xa && !encode_act_map(&tmap_x, a.xa, a.M, a.K)) return kErrCuda;
     if (!encode_operand_map(&tmap_a, a.a, a.M, a.K, 0, BM)) return kErrCuda;
     if (!encode_operand_map(&tmap_b, a.b, a.N, a.K, a.offsets ? a.G : 0, BN)) return kErrCuda;
     if (!encode_output_map(&tmap_d, a.d, a.M, a.N, a.out_bf16 != 0)) return kErrCuda;
@@ -745,17 +945,40 @@ int launch_gemm(const GemmArgs& a, int num_sms, int* status_word, cudaStream_t s
     p.m_fastest = a.offsets ? 0 : 1;
     p.status = status_word;
     p.limit_ns = a.wait_limit_ns;
+    p.qa = reinterpret_cast<uint2*>(const_cast<uint8_t*>(a.a));
+    p.sa_out = const_cast<float*>(a.sa);
+    p.band_flags = a.band_flags;
     const int64_t tiles = (a.M / BM) * ((a.N + BN - 1) / BN);
     const int64_t grid = tiles < num_sms ? tiles : num_sms;
     if (grid <= 0) return kOk;
     // the kernel counts a CTA's K chunks (over all its tiles) in 32 bits
     if ((tiles + grid - 1) / grid * (a.K / BK) >= (int64_t(1) << 31)) return kErrInvalidArg;
+    if (a.xa) {
+        // fused A quantization: the band counters start at zero, and every
+        // CTA waits for the others' share of A, so all must be resident at
+        // once -- a cooperative launch, which the runtime refuses otherwise
+        if ((*cuda_err = cudaMemsetAsync(a.band_flags, 0, static_cast<size_t>(a.M / BM) * sizeof(int32_t),
+                                         stream)) != cudaSuccess)
+            return kErrCuda;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(grid));
+        cfg.blockDim = dim3(THREADS);
+        cfg.dynamicSmemBytes = smem_bytes<0>();
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeCooperative;
+        attr[0].val.cooperative = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        *cuda_err = cudaLaunchKernelEx(&cfg, gemm_blockscaled_kernel<0, true>, tmap_a, tmap_b, tmap_d, tmap_x, p);
+        return *cuda_err == cudaSuccess ? kOk : kErrCuda;
+    }
     if (a.bscale == 1)
-        gemm_blockscaled_kernel<1><<<static_cast<unsigned>(grid), THREADS, smem_bytes<1>(), stream>>>(tmap_a, tmap_b,
-                                                                                                      tmap_d, p);
+        gemm_blockscaled_kernel<1, false><<<static_cast<unsigned>(grid), THREADS, smem_bytes<1>(), stream>>>(
+            tmap_a, tmap_b, tmap_d, tmap_x, p);
     else
-        gemm_blockscaled_kernel<0><<<static_cast<unsigned>(grid), THREADS, smem_bytes<0>(), stream>>>(tmap_a, tmap_b,
-                                                                                                      tmap_d, p);
+        gemm_blockscaled_kernel<0, false><<<static_cast<unsigned>(grid), THREADS, smem_bytes<0>(), stream>>>(
+            tmap_a, tmap_b, tmap_d, tmap_x, p);
     *cuda_err = cudaPeekAtLastError();
     return *cuda_err == cudaSuccess ? kOk : kErrCuda;
 }

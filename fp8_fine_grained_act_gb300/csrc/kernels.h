@@ -45,6 +45,12 @@ struct GemmArgs {
     const int32_t* offsets;   // grouped: device int32[G+1]; nullptr for a dense GEMM
     int G;
     uint64_t wait_limit_ns;   // limit of the kernel's bounded waits
+    // fused A quantization (block B scales, dense only): when xa is set the
+    // kernel first writes the 1x128 codes of the BF16 xa[M, K] to a (as
+    // uint8_t*) and their scales to sa, then runs the GEMM on them;
+    // band_flags: device int32[M/128], zeroed by the launcher
+    const void* xa;
+    int32_t* band_flags;
 };
 
 // Returns a library status code; `cuda_err` receives the CUDA error when the

@@ -72,6 +72,22 @@ FP8FG_DEV bool mbar_wait_bounded(uint32_t bar, uint32_t parity, volatile int* ab
     }
 }
 
+// ------------------------------------------- global flags across CTAs ---
+
+// Acquire load of a global counter at GPU scope (another CTA's release).
+FP8FG_DEV int ld_acquire_gpu(const int* p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+// Release increment of a global counter at GPU scope.
+FP8FG_DEV void red_release_gpu_add(int* p, int v) {
+    asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// Order this thread's generic-proxy global accesses with its async-proxy
+// (TMA) accesses.
+FP8FG_DEV void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
+
 // ------------------------------------------------------- named barriers ---
 // bar.arrive / bar.sync on hardware barrier `id` (1..15; 0 is __syncthreads)
 // completing when `kThreads` threads (whole warps) have arrived.  bar.sync
@@ -139,6 +155,13 @@ FP8FG_DEV void bulk_wait_group_read0() { asm volatile("cp.async.bulk.wait_group.
 FP8FG_DEV void bulk_wait_group0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 // generic-proxy shared-memory writes -> visible to the async proxy (TMA)
 FP8FG_DEV void fence_proxy_async_shared() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+FP8FG_DEV uint4 ld_shared_v4(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr)
+                 : "memory");
+    return v;
+}
 
 FP8FG_DEV void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");

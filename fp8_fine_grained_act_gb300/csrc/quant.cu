@@ -20,84 +20,15 @@
 
 #include "kernels.h"
 #include "ptx.cuh"
+#include "quant_math.cuh"
 
 namespace fp8fg {
 namespace {
 
-constexpr int kGroup = 128;
-
-FP8FG_DEV float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
-FP8FG_DEV float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
-
-// Division by the group scale.  The element code needs fl32(x / s) exactly
-// (an IEEE round-to-nearest quotient).  For a normal scale it is computed
-// with the reciprocal correction of Markstein ("Computation of elementary
-// functions on the IBM RISC System/6000 processor", IBM J. Res. Dev. 1990):
-// with r = RN(1/s) (correctly rounded reciprocal, computed once per group)
-// and q = RN(x r), which is within one ulp of x / s, the remainder
-// x - s q is exact in one FMA and RN(q + (x - s q) r) is the correctly
-// rounded quotient.  The remainder stays exact (no underflow) whenever
-// |x / s| >= 2^-11 and s >= 2^-90; smaller quotients all encode to a signed
-// zero in E4M3 (its smallest magnitude is 2^-9, the tie to zero at 2^-10),
-// and the sign of the quotient is the sign of x (s > 0), which quant4 puts
-// into the codes.  Scales below 2^-90 fall back to the full IEEE division.
-// Bit-exactness against the oracle's IEEE division is tested.
-struct GroupScale {
-    float s, r;
-    int mode;  // 0: s == 0 (codes keep only the sign), 1: reciprocal correction, 2: IEEE division
-    FP8FG_DEV explicit GroupScale(float scale) : s(scale), r(0.0f) {
-        if (s == 0.0f) {
-            mode = 0;
-        } else if (s >= 0x1p-90f) {
-            mode = 1;
-            r = __frcp_rn(s);
-        } else {
-            mode = 2;
-        }
-    }
-};
-
-// Four values -> four E4M3 codes (x0 in the lowest byte).  The quotients by
-// the reciprocal correction are computed two lanes at a time (packed FP32;
-// each lane rounds exactly as the scalar operations).  The sign of each code
-// is taken from x's sign bit, ORed in at the end: a nonzero quotient already
-// carries x's sign, and a quotient that rounds to zero must encode as a signed
-// zero (0x80 for negative x), which is what the OR gives.  A zero scale leaves
-// only the signs.  `signs` holds x_k's sign bit at bit 8k+7.
-FP8FG_DEV uint32_t quant4(float x0, float x1, float x2, float x3, uint32_t signs, const GroupScale& g) {
-    if (g.mode == 0) return signs;
-    uint32_t lo, hi;
-    if (g.mode == 1) {
-        // q = RN(x r); rem = x - s q (exact, one FMA); q' = RN(q + rem r)
-        float q0 = x0, q1 = x1, q2 = x2, q3 = x3;
-        mul2(q0, q1, g.r, g.r);
-        mul2(q2, q3, g.r, g.r);
-        float e0 = x0, e1 = x1, e2 = x2, e3 = x3;
-        fma2(e0, e1, q0, q1, -g.s, -g.s);
-        fma2(e2, e3, q2, q3, -g.s, -g.s);
-        fma2(q0, q1, e0, e1, g.r, g.r);
-        fma2(q2, q3, e2, e3, g.r, g.r);
-        lo = cvt_e4m3x2(q0, q1);
-        hi = cvt_e4m3x2(q2, q3);
-    } else {
-        lo = cvt_e4m3x2(__fdiv_rn(x0, g.s), __fdiv_rn(x1, g.s));
-        hi = cvt_e4m3x2(__fdiv_rn(x2, g.s), __fdiv_rn(x3, g.s));
-    }
-    return (lo | (hi << 16)) | signs;
-}
-
-// Four FP32 values.
-FP8FG_DEV uint32_t quant_quad(float a, float b, float c, float d, const GroupScale& g) {
-    const uint32_t ab = __byte_perm(__float_as_uint(a), __float_as_uint(b), 0x0073);
-    const uint32_t cd = __byte_perm(__float_as_uint(c), __float_as_uint(d), 0x0073);
-    return quant4(a, b, c, d, __byte_perm(ab, cd, 0x5410) & 0x80808080u, g);
-}
-
-// Four BF16 values in two words (value 2i in the low half of word i, 2i+1 in
-// the high half); the high byte of each BF16 value holds its sign bit.
-FP8FG_DEV uint32_t quant_quad_bf16(uint32_t w0, uint32_t w1, const GroupScale& g) {
-    return quant4(bf16_lo(w0), bf16_hi(w0), bf16_lo(w1), bf16_hi(w1), __byte_perm(w0, w1, 0x7531) & 0x80808080u, g);
-}
+// bf16_lo / bf16_hi, GroupScale (the division by the group scale),
+// quant4 / quant_quad / quant_quad_bf16 (four values to four codes) and
+// quad_amax_bf16: quant_math.cuh, shared with the GEMM's fused activation
+// quantizer so that both write the same codes.
 
 // Max |x| of the 128 BF16 values a half-warp holds (8 per lane).  For
 // non-negative BF16 bit patterns the integer order is the numeric order, so
@@ -123,21 +54,6 @@ FP8FG_DEV float group_amax_bf16(const uint4& v) {
 // consecutive rows are contiguous in scales[c * rows + r].
 constexpr int kRowU = 2;
 constexpr int kRowsPerCta = 64 * kRowU;
-
-// Max |x| of the 128 BF16 values a lane quad holds (32 per lane), as in
-// group_amax_bf16.
-FP8FG_DEV float quad_amax_bf16(const uint4 (&v)[4]) {
-    uint32_t m = 0;
-#pragma unroll
-    for (int k = 0; k < 4; ++k)
-        m = __vmaxu2(m, __vmaxu2(__vmaxu2(v[k].x & 0x7FFF7FFFu, v[k].y & 0x7FFF7FFFu),
-                                 __vmaxu2(v[k].z & 0x7FFF7FFFu, v[k].w & 0x7FFF7FFFu)));
-    // xor < 4 stays inside the quad that owns the group
-    m = __vmaxu2(m, __shfl_xor_sync(0xffffffffu, m, 2));
-    m = __vmaxu2(m, __shfl_xor_sync(0xffffffffu, m, 1));
-    const uint32_t hi = m >> 16, lo = m & 0xFFFFu;
-    return __uint_as_float((hi > lo ? hi : lo) << 16);
-}
 
 __global__ void __launch_bounds__(256) quant_act_rows_kernel(const uint4* __restrict__ x, int64_t rows,
                                                              int64_t cols, uint2* __restrict__ q,
@@ -165,13 +81,16 @@ __global__ void __launch_bounds__(256) quant_act_rows_kernel(const uint4* __rest
         const float s = __fdiv_rn(amax, 448.0f);
         const GroupScale gs(s);
         uint2* dst = q + (r * cols + c * kGroup) / 8 + j;
+        with_mode(gs, [&](auto md) {
+            constexpr int kM = decltype(md)::value;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            uint2 out;
-            out.x = quant_quad_bf16(v[u][k].x, v[u][k].y, gs);
-            out.y = quant_quad_bf16(v[u][k].z, v[u][k].w, gs);
-            __stcs(dst + 4 * k, out);
-        }
+            for (int k = 0; k < 4; ++k) {
+                uint2 out;
+                out.x = quant_quad_bf16<kM>(v[u][k].x, v[u][k].y, gs);
+                out.y = quant_quad_bf16<kM>(v[u][k].z, v[u][k].w, gs);
+                __stcs(dst + 4 * k, out);
+            }
+        });
         if (j == 0) scales[c * rows + r] = s;
     }
 }
@@ -238,21 +157,27 @@ __global__ void __launch_bounds__(256) quant_act_cols_kernel(const uint4* __rest
         const GroupScale g0(s0), g1(s1);
         const int64_t ch0 = c0 + 2 * cp;
         if (ch0 < cols) {
-            uint4 o;
-            o.x = quant_quad(lo[0], lo[1], lo[2], lo[3], g0);
-            o.y = quant_quad(lo[4], lo[5], lo[6], lo[7], g0);
-            o.z = quant_quad(lo[8], lo[9], lo[10], lo[11], g0);
-            o.w = quant_quad(lo[12], lo[13], lo[14], lo[15], g0);
-            __stcs(reinterpret_cast<uint4*>(q + ch0 * rows + r0 + 16 * rs), o);
+            with_mode(g0, [&](auto md) {
+                constexpr int kM = decltype(md)::value;
+                uint4 o;
+                o.x = quant_quad<kM>(lo[0], lo[1], lo[2], lo[3], g0);
+                o.y = quant_quad<kM>(lo[4], lo[5], lo[6], lo[7], g0);
+                o.z = quant_quad<kM>(lo[8], lo[9], lo[10], lo[11], g0);
+                o.w = quant_quad<kM>(lo[12], lo[13], lo[14], lo[15], g0);
+                __stcs(reinterpret_cast<uint4*>(q + ch0 * rows + r0 + 16 * rs), o);
+            });
             if (rs == 0) scales[tb * cols + ch0] = s0;
         }
         if (ch0 + 1 < cols) {
-            uint4 o;
-            o.x = quant_quad(hi[0], hi[1], hi[2], hi[3], g1);
-            o.y = quant_quad(hi[4], hi[5], hi[6], hi[7], g1);
-            o.z = quant_quad(hi[8], hi[9], hi[10], hi[11], g1);
-            o.w = quant_quad(hi[12], hi[13], hi[14], hi[15], g1);
-            __stcs(reinterpret_cast<uint4*>(q + (ch0 + 1) * rows + r0 + 16 * rs), o);
+            with_mode(g1, [&](auto md) {
+                constexpr int kM = decltype(md)::value;
+                uint4 o;
+                o.x = quant_quad<kM>(hi[0], hi[1], hi[2], hi[3], g1);
+                o.y = quant_quad<kM>(hi[4], hi[5], hi[6], hi[7], g1);
+                o.z = quant_quad<kM>(hi[8], hi[9], hi[10], hi[11], g1);
+                o.w = quant_quad<kM>(hi[12], hi[13], hi[14], hi[15], g1);
+                __stcs(reinterpret_cast<uint4*>(q + (ch0 + 1) * rows + r0 + 16 * rs), o);
+            });
             if (rs == 0) scales[tb * cols + ch0 + 1] = s1;
         }
         __syncthreads();  // tile and part are reused by the next tile
@@ -299,8 +224,11 @@ __global__ void __launch_bounds__(256, 5) quant_act_dual_kernel(const uint4* __r
         const float s = __fdiv_rn(amax, 448.0f);
         const GroupScale gs(s);
         uint2 out;
-        out.x = quant_quad_bf16(v.x, v.y, gs);
-        out.y = quant_quad_bf16(v.z, v.w, gs);
+        with_mode(gs, [&](auto md) {
+            constexpr int kM = decltype(md)::value;
+            out.x = quant_quad_bf16<kM>(v.x, v.y, gs);
+            out.y = quant_quad_bf16<kM>(v.z, v.w, gs);
+        });
         __stcs(q_row + ((r0 + r) * cols + c0) / 8 + l16, out);
         if (l16 == 0) s_row[cb * rows + r0 + r] = s;
     }
@@ -328,18 +256,25 @@ __global__ void __launch_bounds__(256, 5) quant_act_dual_kernel(const uint4* __r
         uint32_t w[16];
 #pragma unroll
         for (int r = 0; r < 16; ++r) w[r] = tile[32 * rs + 16 * k + r][cp];
-        uint4 o;
         // channel 2cp: the low halves of four consecutive tokens' words
-        o.x = quant_quad(bf16_lo(w[0]), bf16_lo(w[1]), bf16_lo(w[2]), bf16_lo(w[3]), g0);
-        o.y = quant_quad(bf16_lo(w[4]), bf16_lo(w[5]), bf16_lo(w[6]), bf16_lo(w[7]), g0);
-        o.z = quant_quad(bf16_lo(w[8]), bf16_lo(w[9]), bf16_lo(w[10]), bf16_lo(w[11]), g0);
-        o.w = quant_quad(bf16_lo(w[12]), bf16_lo(w[13]), bf16_lo(w[14]), bf16_lo(w[15]), g0);
-        __stcs(dst0 + k, o);
-        o.x = quant_quad(bf16_hi(w[0]), bf16_hi(w[1]), bf16_hi(w[2]), bf16_hi(w[3]), g1);
-        o.y = quant_quad(bf16_hi(w[4]), bf16_hi(w[5]), bf16_hi(w[6]), bf16_hi(w[7]), g1);
-        o.z = quant_quad(bf16_hi(w[8]), bf16_hi(w[9]), bf16_hi(w[10]), bf16_hi(w[11]), g1);
-        o.w = quant_quad(bf16_hi(w[12]), bf16_hi(w[13]), bf16_hi(w[14]), bf16_hi(w[15]), g1);
-        __stcs(dst1 + k, o);
+        with_mode(g0, [&](auto md) {
+            constexpr int kM = decltype(md)::value;
+            uint4 o;
+            o.x = quant_quad<kM>(bf16_lo(w[0]), bf16_lo(w[1]), bf16_lo(w[2]), bf16_lo(w[3]), g0);
+            o.y = quant_quad<kM>(bf16_lo(w[4]), bf16_lo(w[5]), bf16_lo(w[6]), bf16_lo(w[7]), g0);
+            o.z = quant_quad<kM>(bf16_lo(w[8]), bf16_lo(w[9]), bf16_lo(w[10]), bf16_lo(w[11]), g0);
+            o.w = quant_quad<kM>(bf16_lo(w[12]), bf16_lo(w[13]), bf16_lo(w[14]), bf16_lo(w[15]), g0);
+            __stcs(dst0 + k, o);
+        });
+        with_mode(g1, [&](auto md) {
+            constexpr int kM = decltype(md)::value;
+            uint4 o;
+            o.x = quant_quad<kM>(bf16_hi(w[0]), bf16_hi(w[1]), bf16_hi(w[2]), bf16_hi(w[3]), g1);
+            o.y = quant_quad<kM>(bf16_hi(w[4]), bf16_hi(w[5]), bf16_hi(w[6]), bf16_hi(w[7]), g1);
+            o.z = quant_quad<kM>(bf16_hi(w[8]), bf16_hi(w[9]), bf16_hi(w[10]), bf16_hi(w[11]), g1);
+            o.w = quant_quad<kM>(bf16_hi(w[12]), bf16_hi(w[13]), bf16_hi(w[14]), bf16_hi(w[15]), g1);
+            __stcs(dst1 + k, o);
+        });
     }
     if (rs == 0) {
         s_col[tb * cols + ch0] = s0;
@@ -353,7 +288,9 @@ __global__ void __launch_bounds__(256, 5) quant_act_dual_kernel(const uint4* __r
 // 64 + 4(t/32)+{0..3}.  Block amax: warp shuffles, then 16 partials in
 // shared memory.  The optional transposed copy goes through a shared tile of
 // 4x4-byte-transposed words.
-__global__ void __launch_bounds__(512) quant_w_kernel(const float4* __restrict__ w, int64_t rows, int64_t cols,
+// (Two CTAs per SM, i.e. at most 64 registers: at 65 the SM holds one CTA
+// and the kernel ran a third slower.)
+__global__ void __launch_bounds__(512, 2) quant_w_kernel(const float4* __restrict__ w, int64_t rows, int64_t cols,
                                                       uint32_t* __restrict__ q, uint8_t* __restrict__ q_t,
                                                       float* __restrict__ scales) {
     __shared__ float red[16];
@@ -386,7 +323,11 @@ __global__ void __launch_bounds__(512) quant_w_kernel(const float4* __restrict__
         const GroupScale gs(s);
         uint32_t code[8];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) code[k] = quant_quad(v[k].x, v[k].y, v[k].z, v[k].w, gs);
+        with_mode(gs, [&](auto md) {
+            constexpr int kM = decltype(md)::value;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) code[k] = quant_quad<kM>(v[k].x, v[k].y, v[k].z, v[k].w, gs);
+        });
 #pragma unroll
         for (int h = 0; h < 2; ++h)
 #pragma unroll

@@ -170,6 +170,39 @@ int fp8_gemm_blockscaled(const uint8_t *a, const float *sa,
                          cudaStream_t stream);
 
 /*
+ * fp8_gemm_quant_a -- the activation quantizer fused into the GEMM: one
+ * launch computes what fp8_quant_act_1x128 (axis FP8FG_AXIS_COLS) on the BF16
+ * A operand followed by fp8_gemm_blockscaled with 128x128 block B scales
+ * computes, bit for bit (Fprop Y = X W^T and Dgrad dX = dY W of "DeepSeek
+ * FP8 Training", with the 1x128 activation groups of the DeepSeek-V3 FP8
+ * post's Figure 7 (a)).  A persistent kernel quantizes every 128-row band of
+ * A once -- each CTA a share of the 128x128 tiles -- into q_a / s_a, then,
+ * once every band is complete, runs the block-scaled GEMM on them; the
+ * quantized A is not re-read by a second launch and usually still sits in
+ * L2 when the GEMM's TMA loads it.
+ *   a_bf16[M, K] BF16 (16-byte aligned);
+ *   q_a[M, K] uint8 and s_a[K/128, M] float32: OUTPUTS, written with the
+ *     codes and scales of fp8_quant_act_1x128 (q_a 16-byte, s_a 4-byte
+ *     aligned);
+ *   b[N, K], sb, sb_stride_n, sb_stride_k, d, out_dtype: as
+ *     fp8_gemm_blockscaled with FP8FG_BSCALE_BLOCK128;
+ *   band_flags: DEVICE int32[M/128] workspace owned by the caller (4-byte
+ *     aligned), one counter per 128-row band of A; the call zeroes it on
+ *     `stream` before the kernel, so its contents on entry do not matter and
+ *     it must not be used by another call running at the same time.
+ * Requires M, N, K multiples of 128.  The kernel is launched cooperatively
+ * (every CTA resident at once, one per SM): a device or context that cannot
+ * host that gives FP8FG_ERR_CUDA.  Its wait for the other CTAs' share of A
+ * is bounded (fp8fg_set_wait_limit; FP8FG_ERR_TIMEOUT in the device status
+ * word, nothing computed).  M == 0 is a no-op; N == 0 only quantizes A;
+ * K == 0 writes D = 0.  Other errors as fp8_gemm_blockscaled.
+ */
+int fp8_gemm_quant_a(const void *a_bf16, uint8_t *q_a, float *s_a,
+                     const uint8_t *b, const float *sb, int64_t sb_stride_n, int64_t sb_stride_k,
+                     void *d, int out_dtype, int64_t M, int64_t N, int64_t K,
+                     int32_t *band_flags, cudaStream_t stream);
+
+/*
  * fp8_gemm_grouped -- grouped MoE-expert GEMM: rows [off[g], off[g+1]) of A
  * multiply expert weight g: D[r, :] = A[r, :] . B[g]^T with 128x128 block
  * scales (MoE training with FP8 activations, DeepSeek-V3 FP8 post; one

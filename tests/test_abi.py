@@ -206,3 +206,25 @@ def test_gemm_bindings_check_every_operand_before_any_call(lib):
     # (N/128 - 1) * stride_n + (K/128 - 1) * stride_k
     with pytest.raises(ValueError):
         b._need_flat(torch.zeros(3), torch.float32, 4, "sb", torch.device("cpu"))
+
+
+def test_fused_gemm_argument_checks(lib):
+    f = lib.fp8_gemm_quant_a
+    ok = dict(x=A16, qa=A16, sa=A16, b=A16, sb=A16, sn=1, sk=1, d=A16, od=1, M=128, N=128, K=128, fl=A16)
+
+    def call(**kw):
+        v = dict(ok, **kw)
+        return f(v["x"], v["qa"], v["sa"], v["b"], v["sb"], v["sn"], v["sk"], v["d"], v["od"], v["M"], v["N"],
+                 v["K"], v["fl"], None)
+
+    assert call(M=100) == 1 and call(N=200) == 1 and call(K=130) == 1 and call(od=9) == 1
+    assert call(sn=-1) == 1
+    assert call(x=None) == 1 and call(qa=None) == 1 and call(sa=None) == 1 and call(fl=None) == 1
+    assert call(b=None) == 1 and call(d=None) == 1
+    assert call(x=MIS) == 2 and call(qa=MIS) == 2 and call(sa=MIS2) == 2 and call(fl=MIS2) == 2
+    assert call(d=MIS) == 2 and call(b=MIS) == 2
+    assert call(M=0, x=None, qa=None, sa=None, b=None, sb=None, d=None, fl=None) == 0    # empty: no-op
+    if not _has_gpu():
+        assert call() in NOPROBE
+        # K == 0: only d is used, the empty input buffers may be null
+        assert call(K=0, x=None, qa=None, sa=None, b=None, sb=None, fl=None) in NOPROBE
