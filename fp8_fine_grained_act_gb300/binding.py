@@ -26,6 +26,7 @@ FP8FG_ERR_UNSUPPORTED_DEVICE = 3
 FP8FG_ERR_CUDA = 4
 FP8FG_ERR_TIMEOUT = 5
 FP8FG_ERR_TEARDOWN = 6
+FP8FG_ERR_TOO_LARGE = 7
 
 FP8FG_OUT_F32 = 0
 FP8FG_OUT_BF16 = 1
@@ -45,6 +46,7 @@ SIGNATURES = {
     "fp8_gemm_blockscaled": (_i32, [_vp, _vp, _vp, _vp, _i32, _i64, _i64, _vp, _i32, _i64, _i64, _i64, _vp]),
     "fp8_gemm_grouped": (_i32, [_vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i64, _i64, _i64, _vp]),
     "fp8_gemm_quant_a": (_i32, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _vp, _i32, _i64, _i64, _i64, _vp, _vp]),
+    "fp8_gemm_quant_a_noalloc": (_i32, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _vp, _i32, _i64, _i64, _i64, _vp]),
     "fp8fg_status_string": (ctypes.c_char_p, [_i32]),
     "fp8fg_last_device_status": (_i32, [_vp]),
     "fp8fg_selftest_watchdog": (_i32, [_i64, _vp]),

@@ -271,6 +271,9 @@ const char* fp8fg_status_string(int status) {
         case FP8FG_ERR_TIMEOUT: return "FP8FG_ERR_TIMEOUT: a bounded device wait ran out";
         case FP8FG_ERR_TEARDOWN: return "FP8FG_ERR_TEARDOWN: after a failed wait, a kernel's wait for its own copies "
                                         "or MMAs in flight also ran out before it released its resources";
+        case FP8FG_ERR_TOO_LARGE:
+            return "FP8FG_ERR_TOO_LARGE: the problem exceeds a fixed-size library buffer "
+                   "(fp8_gemm_quant_a_noalloc: M must be <= 524288)";
         default: return "FP8FG: unknown status";
     }
 }

@@ -56,9 +56,11 @@ typedef enum {
     FP8FG_ERR_UNSUPPORTED_DEVICE = 3, /* current device is not sm_103 */
     FP8FG_ERR_CUDA = 4,               /* a CUDA runtime/driver call or a launch failed */
     FP8FG_ERR_TIMEOUT = 5,            /* (device status) a bounded wait ran out */
-    FP8FG_ERR_TEARDOWN = 6            /* (device status) after a failed wait, the kernel's bounded wait for its
+    FP8FG_ERR_TEARDOWN = 6,           /* (device status) after a failed wait, the kernel's bounded wait for its
                                          own TMA copies or MMAs in flight ran out too before it freed shared
                                          and tensor memory; replaces an earlier FP8FG_ERR_TIMEOUT */
+    FP8FG_ERR_TOO_LARGE = 7           /* the problem exceeds a fixed-size buffer of the library
+                                         (fp8_gemm_quant_a_noalloc: M > 524288) */
 } fp8fg_status;
 
 typedef enum { FP8FG_OUT_F32 = 0, FP8FG_OUT_BF16 = 1 } fp8fg_out_dtype;
@@ -223,6 +225,38 @@ int fp8_gemm_grouped(const uint8_t *a, const float *sa,
                      const int32_t *group_offsets, int G,
                      void *d, int out_dtype, int64_t M_total, int64_t N, int64_t K,
                      cudaStream_t stream);
+
+/*
+ * fp8_gemm_quant_a_noalloc -- fp8_gemm_quant_a for callers that cannot
+ * allocate its band-counter workspace.  The pages have no counterpart: this
+ * is a service of the library, not a step of the method.
+ *
+ * Who needs it: code that owns no device allocator (a host program or plugin
+ * handed raw device pointers by another runtime, or whose host framework
+ * forbids device allocations behind its own allocator) and code that must
+ * not allocate in its steady state.  The call allocates nothing (no
+ * cudaMalloc or cudaFree, no allocating library routine); instead the
+ * counters live in a fixed array in the library's device memory: 4096 int32
+ * counters (16 KB), held on every GPU that loads the library until the
+ * process exits.
+ *
+ * Arguments, results and errors as fp8_gemm_quant_a (same kernel, same
+ * output, bit for bit), without band_flags; additionally M > 4096 * 128 =
+ * 524288 gives FP8FG_ERR_TOO_LARGE before anything is launched.
+ * The first call on a device looks up the array's device address with
+ * cudaGetSymbolAddress (a runtime call made once per device, with that
+ * device current; FP8FG_ERR_CUDA if it fails): make the first call on each
+ * device before any stream capture begins.
+ * Every call on a device uses the same array, and each call zeroes it on
+ * `stream` before its kernel runs.  Calls whose work overlaps on the GPU
+ * (other streams, or other host threads, without ordering between them)
+ * race on the array and may compute wrong results or fail: order such calls
+ * one after another.
+ */
+int fp8_gemm_quant_a_noalloc(const void *a_bf16, uint8_t *q_a, float *s_a,
+                             const uint8_t *b, const float *sb, int64_t sb_stride_n, int64_t sb_stride_k,
+                             void *d, int out_dtype, int64_t M, int64_t N, int64_t K,
+                             cudaStream_t stream);
 
 /* Human-readable name of a status code (static storage, never NULL). */
 const char *fp8fg_status_string(int status);

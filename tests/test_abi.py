@@ -39,9 +39,18 @@ def test_library_exports_every_declared_symbol(cuda_lib_path):
 def test_status_strings(cuda_lib_path):
     from fp8_fine_grained_act_gb300 import binding as b
     for code, word in [(0, "OK"), (1, "INVALID_ARG"), (2, "MISALIGNED"), (3, "UNSUPPORTED"), (4, "CUDA"),
-                       (5, "TIMEOUT"), (6, "TEARDOWN")]:
+                       (5, "TIMEOUT"), (6, "TEARDOWN"), (7, "TOO_LARGE")]:
         assert word in b.status_string(code)
     assert "unknown" in b.status_string(99)
+
+
+def test_noalloc_rejects_oversize_on_the_host(cuda_lib_path):
+    """More rows than the fixed band-counter array covers is refused before
+    any CUDA call (so this runs without a GPU)."""
+    from fp8_fine_grained_act_gb300 import binding as b
+    st = b.load().fp8_gemm_quant_a_noalloc(None, None, None, None, None, 1, 1, None, b.FP8FG_OUT_BF16,
+                                           4096 * 128 + 128, 128, 128, None)
+    assert st == b.FP8FG_ERR_TOO_LARGE
 
 
 @pytest.fixture(scope="module")
