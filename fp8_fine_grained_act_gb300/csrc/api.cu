@@ -163,8 +163,11 @@ int fp8_gemm_blockscaled(const uint8_t* a, const float* sa, const uint8_t* b, co
     if (M == 0 || N == 0) return kOk;
     if (!d) return kErrInvalidArg;
     if (K > 0 && (!a || !sa || !b || !sb)) return kErrInvalidArg;
-    const bool sb_ok = bscale == FP8FG_BSCALE_ROW ? aligned16(sb) : aligned4(sb);
-    if (!aligned16(d) || (K > 0 && (!aligned16(a) || !aligned4(sa) || !aligned16(b) || !sb_ok)))
+    // per-row B scales: both scale arrays arrive by 16-byte bulk copies
+    const bool row = bscale == FP8FG_BSCALE_ROW;
+    const bool sa_ok = row ? aligned16(sa) : aligned4(sa);
+    const bool sb_ok = row ? aligned16(sb) : aligned4(sb);
+    if (!aligned16(d) || (K > 0 && (!aligned16(a) || !sa_ok || !aligned16(b) || !sb_ok)))
         return kErrMisaligned;
     GemmArgs g{};
     g.a = a;

@@ -106,7 +106,7 @@ constexpr uint64_t kHandoffLimitNs = 3 * kMaxWaitLimitNs;
 constexpr uint64_t kTeardownLimitNs = 10000000ull;
 
 // Shared memory.  kRowB = 1 (B scales per row of B) also keeps a ring of
-// the chunks' B scales.  (Three operand stages measured faster than four on
+// the chunks' B scales and A scales.  (Three operand stages measured faster than four on
 // the Fprop shape: the fourth leaves almost no L1 for the scale loads.)
 template <int kRowB>
 struct __align__(1024) Smem {
@@ -116,6 +116,7 @@ struct __align__(1024) Smem {
     uint8_t b[kStages][B_BYTES];
     uint8_t out[EPI_WARPS][32 * 128];   // per promotion warp: 32 rows x 128 B, 128-byte swizzle
     float sb[kSlots][BN];
+    float sa[kRowB ? kSlots : 1][kRowB ? BM : 4];
     uint64_t full[kStages];
     uint64_t done[kDone];
     uint64_t sfull[kSlots];
@@ -277,8 +278,9 @@ FP8FG_DEV void run_producer(Smem<kRowB>& sm, const CUtensorMap* tmap_a, const CU
                 break;
             }
             const uint32_t sfb = smem_u32(&sm.sfull[sl]);
-            mbar_arrive_expect_tx(sfb, sc_bytes);
+            mbar_arrive_expect_tx(sfb, sc_bytes + BM * 4);
             bulk_load(smem_u32(sm.sb[sl]), p.sb + c * p.N + n0, sc_bytes, sfb);
+            bulk_load(smem_u32(sm.sa[sl]), p.sa + c * p.M + m0, BM * 4, sfb);
             ++g_sc;
         }
     }
@@ -389,30 +391,11 @@ FP8FG_DEV void run_mma(Smem<kRowB>& sm, uint32_t tmem_base, const Params& p, int
 }
 
 // ------------------------------------------------------------ promotion ---
-// acc[0..15] += P[0..15] * scale (block B scales) or
-// acc[0..15] += (P[0..15] * sbv[0..15]) * sa (per-row B scales, sbv loaded
-// into registers before the wait for the TMEM load they are used with).
-template <int kRowB>
-FP8FG_DEV void promote16(float* acc, const uint32_t (&r)[16], float scale, const float4 (&sbv)[4]) {
+// acc[0..15] += P[0..15] * scale (block B scales: one scale per thread and chunk).
+FP8FG_DEV void promote16(float* acc, const uint32_t (&r)[16], float scale) {
 #pragma unroll
-    for (int k = 0; k < 16; k += 2) {
-        float x0 = __uint_as_float(r[k]), x1 = __uint_as_float(r[k + 1]);
-        if (kRowB) {
-            const float4 v = sbv[k / 4];
-            if (k % 4 == 0)
-                mul2(x0, x1, v.x, v.y);
-            else
-                mul2(x0, x1, v.z, v.w);
-        }
-        fma2(acc[k], acc[k + 1], x0, x1, scale, scale);
-    }
-}
-
-// Sixteen per-row B scales of this thread's columns: four 16-byte shared
-// loads, the same address for every lane of the warp (a broadcast).
-FP8FG_DEV void load_sb16(float4 (&v)[4], const float* src) {
-#pragma unroll
-    for (int k = 0; k < 4; ++k) v[k] = reinterpret_cast<const float4*>(src)[k];
+    for (int k = 0; k < 16; k += 2)
+        fma2(acc[k], acc[k + 1], __uint_as_float(r[k]), __uint_as_float(r[k + 1]), scale, scale);
 }
 
 // A tile's origin and the first scales its promotion needs, loaded one tile
@@ -427,7 +410,6 @@ struct TileScales {
     float q[4];             // A scales of chunks 0 .. 3 (a chunk past the tile's last repeats the last)
 };
 
-template <int kRowB>
 FP8FG_DEV TileScales load_tile_scales(int64_t t, const Params& p, int64_t m_tiles, int64_t n_tiles, int64_t kb,
                                       int half, int row, int lane) {
     TileScales ts;
@@ -435,15 +417,12 @@ FP8FG_DEV TileScales load_tile_scales(int64_t t, const Params& p, int64_t m_tile
     tile_origin(t, m_tiles, n_tiles, p.m_fastest, ts.m0, n0);
     ts.col0 = n0 + ECOLS * half;
     ts.active = ts.col0 < p.N;
-    ts.sbp = p.sb;
     ts.sb_cur = 0.0f;
     ts.sb_nxt = 0.0f;
-    if (!kRowB) {
-        const int e = p.offsets ? expert_of(p.offsets, p.G, ts.m0) : 0;
-        ts.sbp = p.sb + e * p.sb_group_stride + (ts.col0 / 128) * p.sb_stride_n;
-        if (ts.active && lane < kb) ts.sb_cur = __ldg(ts.sbp + lane * p.sb_stride_k);
-        if (ts.active && lane + 32 < kb) ts.sb_nxt = __ldg(ts.sbp + (lane + 32) * p.sb_stride_k);
-    }
+    const int e = p.offsets ? expert_of(p.offsets, p.G, ts.m0) : 0;
+    ts.sbp = p.sb + e * p.sb_group_stride + (ts.col0 / 128) * p.sb_stride_n;
+    if (ts.active && lane < kb) ts.sb_cur = __ldg(ts.sbp + lane * p.sb_stride_k);
+    if (ts.active && lane + 32 < kb) ts.sb_nxt = __ldg(ts.sbp + (lane + 32) * p.sb_stride_k);
     ts.sap = p.sa + ts.m0 + row;
     // (indices clamped to the last chunk instead of a select on the loaded
     // value: a select would make the thread wait for the load to return)
@@ -452,10 +431,8 @@ FP8FG_DEV TileScales load_tile_scales(int64_t t, const Params& p, int64_t m_tile
     return ts;
 }
 
-template <int kRowB>
-FP8FG_DEV void run_epilogue(Smem<kRowB>& sm, uint32_t tmem_base, const Params& p, const CUtensorMap* tmap_d,
+FP8FG_DEV void run_epilogue(Smem<0>& sm, uint32_t tmem_base, const Params& p, const CUtensorMap* tmap_d,
                             int64_t m_tiles, int64_t n_tiles, int64_t kb, int warp, int lane) {
-    constexpr int SL = Smem<kRowB>::kSlots;
     volatile int* abort_flag = &sm.abort_flag;
     const int quad = warp & 3;          // TMEM lanes this warp may read: 32*quad .. 32*quad+31
     const int half = (warp - 4) >> 2;   // columns ECOLS*half .. ECOLS*half+ECOLS-1 of the tile
@@ -466,7 +443,7 @@ FP8FG_DEV void run_epilogue(Smem<kRowB>& sm, uint32_t tmem_base, const Params& p
     uint32_t g = 0;
     bool dead = false;   // after a failed wait: no work, but still one hand-back per chunk
     bool timed_out = false;
-    TileScales nts = load_tile_scales<kRowB>(blockIdx.x, p, m_tiles, n_tiles, kb, half, row, lane);
+    TileScales nts = load_tile_scales(blockIdx.x, p, m_tiles, n_tiles, kb, half, row, lane);
     for (int64_t t = blockIdx.x; t < num_tiles; t += gridDim.x) {
         const int64_t m0 = nts.m0, col0 = nts.col0;
         const bool active = nts.active;
@@ -484,8 +461,7 @@ FP8FG_DEV void run_epilogue(Smem<kRowB>& sm, uint32_t tmem_base, const Params& p
         for (int j = 0; j < ECOLS; ++j) acc[j] = 0.0f;
         auto chunk = [&](int64_t c, float& qa) {
             const uint32_t buf = g % NBUF;
-            const uint32_t sl = g % SL, sph = (g / SL) & 1;
-            if (!kRowB && c > 0 && (c & 31) == 0) {
+            if (c > 0 && (c & 31) == 0) {
                 sb_cur = sb_nxt;
                 if (active) sb_nxt = __ldg(sbp + min(c + 32 + lane, kb - 1) * p.sb_stride_k);
             }
@@ -509,42 +485,28 @@ FP8FG_DEV void run_epilogue(Smem<kRowB>& sm, uint32_t tmem_base, const Params& p
                 dead = true;
                 timed_out = true;
             }
-            if (kRowB && !dead) {
-                ok = mbar_wait_bounded(smem_u32(&sm.sfull[sl]), sph, abort_flag, p.status, p.limit_ns, kErrTimeout);
-                if (!__all_sync(0xffffffffu, ok)) dead = true;
-            }
             tc_fence_after();
             const float sbv = __shfl_sync(0xffffffffu, sb_cur, static_cast<int>(c & 31));
             if (active && !dead) {
                 const uint32_t taddr = tmem_base + t_lane + buf * BN + ECOLS * half;
-                const float scale = kRowB ? sa_i : sa_i * sbv;
-                const float* sbrow = sm.sb[sl] + ECOLS * half;
+                const float scale = sa_i * sbv;
                 // ECOLS / 16 loads of 16 columns; the next load is in flight
                 // while the previous 16 columns are folded in (16, not 32:
-                // with 32 the registers spilled).  Per-row B scales: the next
-                // slice's 16 scales are loaded before the wait for the next
-                // TMEM load, so that no shared-memory load sits between a
-                // TMEM wait and the arithmetic it feeds.
+                // with 32 the registers spilled)
                 constexpr int NJ = ECOLS / 16;
                 uint32_t r[2][16];
-                float4 sv[4];
-                if (kRowB) load_sb16(sv, sbrow);
                 tmem_ld_32x32b_x16(taddr, r[0]);
                 tmem_ld_wait(r[0]);
 #pragma unroll
                 for (int j = 0; j < NJ; ++j) {
                     if (j + 1 < NJ) tmem_ld_32x32b_x16(taddr + 16 * (j + 1), r[(j + 1) & 1]);
-                    promote16<kRowB>(acc + 16 * j, r[j & 1], scale, sv);
-                    if (j + 1 < NJ) {
-                        if (kRowB) load_sb16(sv, sbrow + 16 * (j + 1));
-                        tmem_ld_wait(r[(j + 1) & 1]);
-                    }
+                    promote16(acc + 16 * j, r[j & 1], scale);
+                    if (j + 1 < NJ) tmem_ld_wait(r[(j + 1) & 1]);
                 }
             }
             // the buffer goes back only after the loaded registers are consumed
             tc_fence_before();
             named_arrive<kRelThreads>(1 + static_cast<int>(buf));
-            if (kRowB && !dead && lane == 0) mbar_arrive(smem_u32(&sm.sempty[sl]));
             ++g;
         };
         for (int64_t c = 0; c < kb; c += 4) {
@@ -554,7 +516,7 @@ FP8FG_DEV void run_epilogue(Smem<kRowB>& sm, uint32_t tmem_base, const Params& p
             if (c + 3 < kb) chunk(c + 3, qa3);
         }
         if (t + gridDim.x < num_tiles)
-            nts = load_tile_scales<kRowB>(t + gridDim.x, p, m_tiles, n_tiles, kb, half, row, lane);
+            nts = load_tile_scales(t + gridDim.x, p, m_tiles, n_tiles, kb, half, row, lane);
         if (!active || dead) continue;
         // 32 rows x 128 columns of this warp -> shared memory (row = lane,
         // 16-byte chunk k of each 128-byte row at k ^ (row & 7): the 128-byte
@@ -590,6 +552,171 @@ FP8FG_DEV void run_epilogue(Smem<kRowB>& sm, uint32_t tmem_base, const Params& p
                 __syncwarp();
                 if (lane == 0) {
                     tma_store_2d(tmap_d, ob, static_cast<int32_t>(col0 + (p.out_bf16 ? 64 : 32) * rd), gy);
+                    bulk_commit_group();
+                }
+            }
+        }
+    }
+    if (lane == 0) bulk_wait_group0();   // every store of this warp has completed
+    __syncwarp();
+}
+
+// ---------------------------------------- promotion, per-row B scales ---
+// Per-row B scales (Wgrad: both operands scaled per 128-token chunk, one
+// scale per output row i and one per output column j): every partial sum
+// takes its own product sa_i * sb_j, two FP32 operations per sum.  The
+// chunk's B and A scales arrive in shared memory with the chunk (the
+// producer's bulk copies).  TMEM is read with the 16x256b shape, so that a
+// thread holds 4 rows x 32 columns of its warp's 32 x 128 block and needs 32
+// B scales and 4 A scales per chunk: a thread that held one whole row would
+// need all 128 of its columns' B scales every chunk.  Shared-memory loads
+// compete with the tensor core, which streams its operands from shared
+// memory (each load wavefront delays the MMAs), so their number matters
+// more than their latency.
+//
+// Thread (g = lane / 4, q = lane % 4) of promotion warp (quad, half):
+//   rows    32 quad + 16 rh + 8 rr + g          (rh, rr in {0, 1})
+//   columns ECOLS half + 8 b + 2 q + e          (b < 16, e in {0, 1})
+// TMEM load j (0..7) reads the 16 rows of rh = j % 2 and the column blocks
+// b = 4 (j / 2) + bb (bb < 4); its register 4 bb + 2 rr + e is folded into
+// acc[16 j + 4 bb + 2 rr + e].
+FP8FG_DEV void run_epilogue_rowb(Smem<1>& sm, uint32_t tmem_base, const Params& p, const CUtensorMap* tmap_d,
+                                 int64_t m_tiles, int64_t n_tiles, int64_t kb, int warp, int lane) {
+    constexpr int SL = Smem<1>::kSlots;
+    volatile int* abort_flag = &sm.abort_flag;
+    const int quad = warp & 3;          // TMEM lanes this warp may read: 32*quad .. 32*quad+31
+    const int half = (warp - 4) >> 2;   // columns ECOLS*half .. ECOLS*half+ECOLS-1 of the tile
+    const int g4 = lane >> 2, q = lane & 3;
+    const uint32_t ob = smem_u32(sm.out[warp - 4]);
+    const int64_t num_tiles = m_tiles * n_tiles;
+    uint32_t g = 0;
+    bool dead = false;   // after a failed wait: no work, but still one hand-back per chunk
+    bool timed_out = false;
+    for (int64_t t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+        int64_t m0, n0;
+        tile_origin(t, m_tiles, n_tiles, p.m_fastest, m0, n0);
+        const int64_t col0 = n0 + ECOLS * half;
+        const bool active = col0 < p.N;
+        float acc[ECOLS];
+#pragma unroll
+        for (int j = 0; j < ECOLS; ++j) acc[j] = 0.0f;
+        for (int64_t c = 0; c < kb; ++c) {
+            const uint32_t buf = g % NBUF;
+            const uint32_t sl = g % SL, sph = (g / SL) & 1;
+            // (the waits as in run_epilogue)
+            bool ok = wait_plain(smem_u32(&sm.done[g & (kDone - 1)]), (g / kDone) & 1,
+                                 timed_out ? 1000000ull : kHandoffLimitNs);
+            if (!__all_sync(0xffffffffu, ok)) {
+                if (lane == 0) {
+                    atomicCAS(p.status, 0, kErrTimeout);
+                    *abort_flag = 1;
+                }
+                dead = true;
+                timed_out = true;
+            }
+            if (!dead) {
+                ok = mbar_wait_bounded(smem_u32(&sm.sfull[sl]), sph, abort_flag, p.status, p.limit_ns, kErrTimeout);
+                if (!__all_sync(0xffffffffu, ok)) dead = true;
+            }
+            tc_fence_after();
+            if (active && !dead) {
+                const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + buf * BN + ECOLS * half;
+                const float* sbp = sm.sb[sl] + ECOLS * half + 2 * q;
+                const float* sap = sm.sa[sl] + quad * 32 + g4;
+                float sav[4];   // A scales of rows 8k + g: (rh, rr) = (k / 2, k % 2)
+#pragma unroll
+                for (int k = 0; k < 4; ++k) sav[k] = sap[8 * k];
+                float2 sbv[4];  // B scales of the current 32 columns
+#pragma unroll
+                for (int bb = 0; bb < 4; ++bb) sbv[bb] = *reinterpret_cast<const float2*>(sbp + 8 * bb);
+                uint32_t r[2][16];
+                tmem_ld_16x256b_x4(taddr, r[0]);
+                tmem_ld_wait(r[0]);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    if (j + 1 < 8)
+                        tmem_ld_16x256b_x4(taddr + (static_cast<uint32_t>(16 * ((j + 1) & 1)) << 16) +
+                                               32 * ((j + 1) >> 1),
+                                           r[(j + 1) & 1]);
+                    const int rh = j & 1;
+#pragma unroll
+                    for (int bb = 0; bb < 4; ++bb) {
+#pragma unroll
+                        for (int rr = 0; rr < 2; ++rr) {
+                            float x0 = __uint_as_float(r[j & 1][4 * bb + 2 * rr]);
+                            float x1 = __uint_as_float(r[j & 1][4 * bb + 2 * rr + 1]);
+                            mul2(x0, x1, sbv[bb].x, sbv[bb].y);
+                            const float sa_r = sav[2 * rh + rr];
+                            float* a2 = acc + 16 * j + 4 * bb + 2 * rr;
+                            fma2(a2[0], a2[1], x0, x1, sa_r, sa_r);
+                        }
+                    }
+                    if (j + 1 < 8) {
+                        if (j & 1) {   // the next load starts the next 32 columns
+#pragma unroll
+                            for (int bb = 0; bb < 4; ++bb)
+                                sbv[bb] = *reinterpret_cast<const float2*>(sbp + 32 * ((j + 1) >> 1) + 8 * bb);
+                        }
+                        tmem_ld_wait(r[(j + 1) & 1]);
+                    }
+                }
+            }
+            // the buffer goes back only after the loaded registers are consumed
+            tc_fence_before();
+            named_arrive<kRelThreads>(1 + static_cast<int>(buf));
+            __syncwarp();   // every lane's scale loads from the slot are done
+            if (!dead && lane == 0) mbar_arrive(smem_u32(&sm.sempty[sl]));
+            ++g;
+        }
+        if (!active || dead) continue;
+        // 32 rows x 128 columns of this warp -> the warp's staging buffer
+        // (row-major 128-byte rows, 16-byte chunk k of row r at k ^ (r & 7):
+        // the output map's 128-byte swizzle) -> one TMA store per 128 bytes
+        // of row, as in run_epilogue, from this thread's 4 rows x 32 columns.
+        const int32_t gy = static_cast<int32_t>(m0 + quad * 32);
+        if (p.out_bf16) {
+#pragma unroll
+            for (int rd = 0; rd < 2; ++rd) {   // 64 columns per round: blocks b = 8 rd + bp
+                if (lane == 0) bulk_wait_group_read0();
+                __syncwarp();
+#pragma unroll
+                for (int bp = 0; bp < 8; ++bp) {
+                    const int b = 8 * rd + bp;
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const int rh = k >> 1, rr = k & 1, row = 16 * rh + 8 * rr + g4;
+                        const float* a2 = acc + 16 * (2 * (b >> 2) + rh) + 4 * (b & 3) + 2 * rr;
+                        st_shared_u32(ob + static_cast<uint32_t>(row) * 128 + ((bp ^ (row & 7)) << 4) + 4 * q,
+                                      pack_bf16x2(a2[0], a2[1]));
+                    }
+                }
+                fence_proxy_async_shared();
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_2d(tmap_d, ob, static_cast<int32_t>(col0 + 64 * rd), gy);
+                    bulk_commit_group();
+                }
+            }
+        } else {
+#pragma unroll
+            for (int rd = 0; rd < 4; ++rd) {   // 32 columns per round: blocks b = 4 rd + bb
+                if (lane == 0) bulk_wait_group_read0();
+                __syncwarp();
+#pragma unroll
+                for (int bb = 0; bb < 4; ++bb) {
+                    const int kc = 2 * bb + (q >> 1);   // 16-byte chunk of the row
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const int rh = k >> 1, rr = k & 1, row = 16 * rh + 8 * rr + g4;
+                        const float* a2 = acc + 16 * (2 * rd + rh) + 4 * bb + 2 * rr;
+                        st_shared_v2(ob + static_cast<uint32_t>(row) * 128 + ((kc ^ (row & 7)) << 4) + 8 * (q & 1),
+                                     __float_as_uint(a2[0]), __float_as_uint(a2[1]));
+                    }
+                }
+                fence_proxy_async_shared();
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_2d(tmap_d, ob, static_cast<int32_t>(col0 + 32 * rd), gy);
                     bulk_commit_group();
                 }
             }
@@ -821,7 +948,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (warp == 2) run_watch<kRowB>(sm, p, m_tiles, n_tiles, kb, lane);
     } else {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(REGS_HIGH));
-        run_epilogue<kRowB>(sm, tmem_base, p, &tmap_d, m_tiles, n_tiles, kb, warp, lane);
+        if constexpr (kRowB != 0)
+            run_epilogue_rowb(sm, tmem_base, p, &tmap_d, m_tiles, n_tiles, kb, warp, lane);
+        else
+            run_epilogue(sm, tmem_base, p, &tmap_d, m_tiles, n_tiles, kb, warp, lane);
     }
     __syncwarp();
     tc_fence_before();

@@ -157,9 +157,9 @@ int fp8_quant_w_128x128(const float *w, int64_t rows, int64_t cols,
  *   d[M, N]: float32 (out_dtype FP8FG_OUT_F32) or bfloat16 rounded to
  *     nearest even (FP8FG_OUT_BF16).
  * Requires M % 128 == 0, N % 128 == 0, K % 128 == 0 (tokens are padded to
- * 128 by the caller); a, b and d 16-byte aligned, sa 4-byte aligned, sb
- * 4-byte aligned for block scales and 16-byte aligned for per-row B scales
- * (copied in bulk); sb strides >= 0.
+ * 128 by the caller); a, b and d 16-byte aligned; sa and sb 4-byte aligned
+ * for block scales, both 16-byte aligned for per-row B scales (copied in
+ * bulk); sb strides >= 0.
  * K == 0 writes zeros.  M == 0 or N == 0 is a no-op.
  * Accuracy (tested): |d - o| <= 2^-16 * sum_k |a~ b~| for FP32 output, plus
  * one BF16 spacing of o for BF16 output, o being the exact sum of the
