@@ -30,47 +30,34 @@ namespace {
 // quad_amax_bf16: quant_math.cuh, shared with the GEMM's fused activation
 // quantizer so that both write the same codes.
 
-// Max |x| of the 128 BF16 values a half-warp holds (8 per lane).  For
-// non-negative BF16 bit patterns the integer order is the numeric order, so
-// the maximum is taken on the 16-bit patterns with the sign bits cleared,
-// two at a time; the result widens to FP32 exactly.  Inputs are finite.
-FP8FG_DEV float group_amax_bf16(const uint4& v) {
-    uint32_t m = __vmaxu2(__vmaxu2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu), __vmaxu2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu));
-    // xor < 16 stays inside the half-warp that owns the group
-#pragma unroll
-    for (int k = 8; k >= 1; k >>= 1) m = __vmaxu2(m, __shfl_xor_sync(0xffffffffu, m, k));
-    const uint32_t hi = m >> 16, lo = m & 0xFFFFu;
-    return __uint_as_float((hi > lo ? hi : lo) << 16);
-}
-
 // ------------------------------------------------------------ 1 x 128 ----
 // Grid (row blocks, 128-column groups): a CTA owns kRowsPerCta rows of one
 // group column c.  A lane quad owns one row's group (4 lanes x 32 BF16 = 256
-// bytes): lane j of the quad loads the group's 16-byte chunks j, j+4, j+8,
-// j+12, so each load instruction reads 64 contiguous bytes per row and each
-// store writes 32; the group maximum needs two shuffles, and the scale's
-// division and reciprocal are shared by 32 elements per lane.  A warp covers
-// 8 rows per step and keeps kRowU steps' loads in flight; the scales of
-// consecutive rows are contiguous in scales[c * rows + r].
+// bytes): lane j of the quad loads the group's 16-byte chunks 2j, 2j+1,
+// 2j+8, 2j+9, so that its 32 codes are two 16-byte runs of the output row
+// (one 16-byte store each); the group maximum needs two shuffles, and the
+// scale's division and reciprocal are shared by 32 elements per lane.  A warp
+// covers 8 rows per step and keeps kRowU steps' loads in flight; the scales
+// of consecutive rows are contiguous in scales[c * rows + r].
 constexpr int kRowU = 2;
 constexpr int kRowsPerCta = 64 * kRowU;
 
 __global__ void __launch_bounds__(256) quant_act_rows_kernel(const uint4* __restrict__ x, int64_t rows,
-                                                             int64_t cols, uint2* __restrict__ q,
+                                                             int64_t cols, uint4* __restrict__ q,
                                                              float* __restrict__ scales) {
     const int64_t c = blockIdx.y;
-    const int j = threadIdx.x & 3;        // chunks j, j+4, j+8, j+12 of the group
+    const int j = threadIdx.x & 3;        // chunks 2j, 2j+1, 2j+8, 2j+9 of the group
     const int rq = threadIdx.x >> 2;      // row of the quad within a 64-row step
     const int64_t r0 = static_cast<int64_t>(blockIdx.x) * kRowsPerCta + rq;
     uint4 v[kRowU][4];
 #pragma unroll
     for (int u = 0; u < kRowU; ++u) {
         const int64_t r = r0 + 64 * u;
-        const uint4* src = x + (r * cols + c * kGroup) / 8 + j;
+        const uint4* src = x + (r * cols + c * kGroup) / 8 + 2 * j;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
             v[u][k] = make_uint4(0, 0, 0, 0);
-            if (r < rows) v[u][k] = __ldcs(src + 4 * k);
+            if (r < rows) v[u][k] = __ldcs(src + (k & 1) + 8 * (k >> 1));
         }
     }
 #pragma unroll
@@ -80,15 +67,17 @@ __global__ void __launch_bounds__(256) quant_act_rows_kernel(const uint4* __rest
         if (r >= rows) continue;
         const float s = __fdiv_rn(amax, 448.0f);
         const GroupScale gs(s);
-        uint2* dst = q + (r * cols + c * kGroup) / 8 + j;
+        uint4* dst = q + (r * cols + c * kGroup) / 16 + j;
         with_mode(gs, [&](auto md) {
             constexpr int kM = decltype(md)::value;
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                uint2 out;
-                out.x = quant_quad_bf16<kM>(v[u][k].x, v[u][k].y, gs);
-                out.y = quant_quad_bf16<kM>(v[u][k].z, v[u][k].w, gs);
-                __stcs(dst + 4 * k, out);
+            for (int h = 0; h < 2; ++h) {   // chunks 2j + 8h and 2j + 8h + 1
+                uint4 out;
+                out.x = quant_quad_bf16<kM>(v[u][2 * h].x, v[u][2 * h].y, gs);
+                out.y = quant_quad_bf16<kM>(v[u][2 * h].z, v[u][2 * h].w, gs);
+                out.z = quant_quad_bf16<kM>(v[u][2 * h + 1].x, v[u][2 * h + 1].y, gs);
+                out.w = quant_quad_bf16<kM>(v[u][2 * h + 1].z, v[u][2 * h + 1].w, gs);
+                __stcs(dst + 4 * h, out);
             }
         });
         if (j == 0) scales[c * rows + r] = s;
@@ -185,25 +174,134 @@ __global__ void __launch_bounds__(256) quant_act_cols_kernel(const uint4* __rest
 }
 
 // ------------------------------------------------- 1 x 128 and 128 x 1 ----
-// One CTA per 128 x 128 tile of X, 256 threads, 5 CTAs per SM.  The tile
-// (32 KB) is copied into shared memory with cp.async (no registers held
-// while the loads are in flight), then read twice: the row pass gives
-// half-warp h rows h, h+16, ..., h+112 (8 BF16 per lane, the 1x128 amax by
-// half-warp shuffles, codes to q_row); the column pass gives thread t the
-// channel pair t % 64 over 32 tokens (t / 64), the 4 partial maxima meet in
-// shared memory, and each thread writes 2 x 16 codes per channel into
-// q_col_t[cols, rows].  A warp always reads 32 consecutive words of one row,
-// so the unpadded tile has no bank conflicts.  The arithmetic is the same as
-// the single-axis kernels', so both outputs equal theirs bit for bit.  With
-// kRowPass = false it is the 128x1 quantizer alone, used when cols is a
-// multiple of 128 (a staged 1x128-only version measured no faster than
-// quant_act_rows_kernel).
-template <bool kRowPass>
-__global__ void __launch_bounds__(256, 5) quant_act_dual_kernel(const uint4* __restrict__ x, int64_t rows,
-                                                                int64_t cols, uint2* __restrict__ q_row,
+// One CTA per 128 x 128 tile of X, 256 threads.  A lane quad owns one row's
+// 1x128 group in each of two passes (rows q and q + 64 for quad q): lane j
+// loads the group's 16-byte chunks 2j, 2j+1, 2j+8, 2j+9 into registers, so
+// that its 32 codes form two 16-byte runs of the output row (16-byte stores)
+// and the group's amax, division and reciprocal are shared by 32 elements
+// per lane.  The row pass quantizes from those registers; the same registers
+// are written to a shared tile (rows of 64 words + 4 pad words: the two rows
+// of a quarter-warp's 16-byte stores fall on disjoint banks, and a warp
+// reading 32 consecutive words of one row is conflict-free) for the column
+// pass, which gives thread t the channel pair t % 64 over 32 tokens (t / 64);
+// the 4 partial maxima meet in shared memory, and each thread writes 2 x 16
+// codes per channel into q_col_t[cols, rows].  The arithmetic is the same as
+// the single-axis kernels', so both outputs equal theirs bit for bit.
+constexpr int kTileWords = kGroup / 2 + 4;   // padded row of the shared tile
+
+__global__ void __launch_bounds__(256, 4) quant_act_dual_kernel(const uint4* __restrict__ x, int64_t rows,
+                                                                int64_t cols, uint4* __restrict__ q_row,
                                                                 float* __restrict__ s_row,
                                                                 uint8_t* __restrict__ q_col_t,
                                                                 float* __restrict__ s_col) {
+    __shared__ __align__(16) uint32_t tile[kGroup][kTileWords];
+    __shared__ float part[4][kGroup];
+    const int t = threadIdx.x;
+    const int j = t & 3;        // lane of the quad
+    const int rq = t >> 2;      // quad: rows rq and rq + 64 of the tile
+    const int64_t tb = blockIdx.x, cb = blockIdx.y;
+    const int64_t r0 = tb * kGroup, c0 = cb * kGroup;
+    uint4 v[2][4];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+        const uint4* src = x + ((r0 + rq + 64 * u) * cols + c0) / 8 + 2 * j;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) v[u][k] = __ldcs(src + (k & 1) + 8 * (k >> 1));
+    }
+#pragma unroll
+    for (int u = 0; u < 2; ++u)
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            *reinterpret_cast<uint4*>(&tile[rq + 64 * u][4 * (2 * j + (k & 1) + 8 * (k >> 1))]) = v[u][k];
+    {
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int64_t r = r0 + rq + 64 * u;
+            const float amax = quad_amax_bf16(v[u]);
+            const float s = __fdiv_rn(amax, 448.0f);
+            const GroupScale gs(s);
+            uint4 lo, hi;   // codes of chunks 2j, 2j+1 and of chunks 2j+8, 2j+9
+            with_mode(gs, [&](auto md) {
+                constexpr int kM = decltype(md)::value;
+                lo.x = quant_quad_bf16<kM>(v[u][0].x, v[u][0].y, gs);
+                lo.y = quant_quad_bf16<kM>(v[u][0].z, v[u][0].w, gs);
+                lo.z = quant_quad_bf16<kM>(v[u][1].x, v[u][1].y, gs);
+                lo.w = quant_quad_bf16<kM>(v[u][1].z, v[u][1].w, gs);
+                hi.x = quant_quad_bf16<kM>(v[u][2].x, v[u][2].y, gs);
+                hi.y = quant_quad_bf16<kM>(v[u][2].z, v[u][2].w, gs);
+                hi.z = quant_quad_bf16<kM>(v[u][3].x, v[u][3].y, gs);
+                hi.w = quant_quad_bf16<kM>(v[u][3].z, v[u][3].w, gs);
+            });
+            uint4* dst = q_row + (r * cols + c0) / 16 + j;
+            __stcs(dst, lo);
+            __stcs(dst + 4, hi);
+            if (j == 0) s_row[cb * rows + r] = s;
+        }
+    }
+    __syncthreads();
+    const int cp = t & 63;   // channel pair: channels 2cp, 2cp+1 of the tile
+    const int rs = t >> 6;   // token segment: tokens 32rs .. 32rs+31
+    uint32_t m2 = 0;         // both channels' maxima as 16-bit patterns
+#pragma unroll
+    for (int r = 0; r < 32; ++r) m2 = __vmaxu2(m2, tile[32 * rs + r][cp] & 0x7FFF7FFFu);
+    part[rs][2 * cp] = __uint_as_float(m2 << 16);
+    part[rs][2 * cp + 1] = __uint_as_float(m2 & 0xFFFF0000u);
+    __syncthreads();
+    float a0 = part[0][2 * cp], a1 = part[0][2 * cp + 1];
+#pragma unroll
+    for (int k = 1; k < 4; ++k) {
+        a0 = fmaxf(a0, part[k][2 * cp]);
+        a1 = fmaxf(a1, part[k][2 * cp + 1]);
+    }
+    const float s0 = __fdiv_rn(a0, 448.0f), s1 = __fdiv_rn(a1, 448.0f);
+    const GroupScale g0(s0), g1(s1);
+    const int64_t ch0 = c0 + 2 * cp;
+    uint4* dst0 = reinterpret_cast<uint4*>(q_col_t + ch0 * rows + r0 + 32 * rs);
+    uint4* dst1 = reinterpret_cast<uint4*>(q_col_t + (ch0 + 1) * rows + r0 + 32 * rs);
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        uint32_t w[16];
+#pragma unroll
+        for (int r = 0; r < 16; ++r) w[r] = tile[32 * rs + 16 * k + r][cp];
+        // channel 2cp: the low halves of four consecutive tokens' words
+        with_mode(g0, [&](auto md) {
+            constexpr int kM = decltype(md)::value;
+            uint4 o;
+            o.x = quant_quad<kM>(bf16_lo(w[0]), bf16_lo(w[1]), bf16_lo(w[2]), bf16_lo(w[3]), g0);
+            o.y = quant_quad<kM>(bf16_lo(w[4]), bf16_lo(w[5]), bf16_lo(w[6]), bf16_lo(w[7]), g0);
+            o.z = quant_quad<kM>(bf16_lo(w[8]), bf16_lo(w[9]), bf16_lo(w[10]), bf16_lo(w[11]), g0);
+            o.w = quant_quad<kM>(bf16_lo(w[12]), bf16_lo(w[13]), bf16_lo(w[14]), bf16_lo(w[15]), g0);
+            __stcs(dst0 + k, o);
+        });
+        with_mode(g1, [&](auto md) {
+            constexpr int kM = decltype(md)::value;
+            uint4 o;
+            o.x = quant_quad<kM>(bf16_hi(w[0]), bf16_hi(w[1]), bf16_hi(w[2]), bf16_hi(w[3]), g1);
+            o.y = quant_quad<kM>(bf16_hi(w[4]), bf16_hi(w[5]), bf16_hi(w[6]), bf16_hi(w[7]), g1);
+            o.z = quant_quad<kM>(bf16_hi(w[8]), bf16_hi(w[9]), bf16_hi(w[10]), bf16_hi(w[11]), g1);
+            o.w = quant_quad<kM>(bf16_hi(w[12]), bf16_hi(w[13]), bf16_hi(w[14]), bf16_hi(w[15]), g1);
+            __stcs(dst1 + k, o);
+        });
+    }
+    if (rs == 0) {
+        s_col[tb * cols + ch0] = s0;
+        s_col[tb * cols + ch0 + 1] = s1;
+    }
+}
+
+// ------------------------------------------------------------ 128 x 1 ----
+// The 128x1 quantizer alone when cols is a multiple of 128: one CTA per
+// 128 x 128 tile, 256 threads, 5 CTAs per SM.  The tile (32 KB) is copied
+// into shared memory with cp.async (no registers held while the copies are
+// in flight; with no row pass to feed, this beats staging the tile through
+// registers), then the column pass of quant_act_dual_kernel: thread t takes
+// the channel pair t % 64 over 32 tokens (t / 64), the 4 partial maxima meet
+// in shared memory, and each thread writes 2 x 16 codes per channel into
+// q_col_t[cols, rows].  A warp always reads 32 consecutive words of one row,
+// so the unpadded tile has no bank conflicts.
+__global__ void __launch_bounds__(256, 5) quant_act_cols_tile_kernel(const uint4* __restrict__ x, int64_t rows,
+                                                                   int64_t cols, uint8_t* __restrict__ q_col_t,
+                                                                   float* __restrict__ s_col) {
     __shared__ __align__(16) uint32_t tile[kGroup][kGroup / 2];
     __shared__ float part[4][kGroup];
     const int t = threadIdx.x, l16 = t & 15, hw = t >> 4;
@@ -216,22 +314,6 @@ __global__ void __launch_bounds__(256, 5) quant_act_dual_kernel(const uint4* __r
     }
     cp_async_wait_all();
     __syncthreads();
-#pragma unroll 2
-    for (int u = 0; u < (kRowPass ? 8 : 0); ++u) {
-        const int r = hw + 16 * u;
-        const uint4 v = *reinterpret_cast<const uint4*>(&tile[r][4 * l16]);
-        const float amax = group_amax_bf16(v);
-        const float s = __fdiv_rn(amax, 448.0f);
-        const GroupScale gs(s);
-        uint2 out;
-        with_mode(gs, [&](auto md) {
-            constexpr int kM = decltype(md)::value;
-            out.x = quant_quad_bf16<kM>(v.x, v.y, gs);
-            out.y = quant_quad_bf16<kM>(v.z, v.w, gs);
-        });
-        __stcs(q_row + ((r0 + r) * cols + c0) / 8 + l16, out);
-        if (l16 == 0) s_row[cb * rows + r0 + r] = s;
-    }
     const int cp = t & 63;   // channel pair: channels 2cp, 2cp+1 of the tile
     const int rs = t >> 6;   // token segment: tokens 32rs .. 32rs+31
     uint32_t m2 = 0;         // both channels' maxima as 16-bit patterns
@@ -322,7 +404,6 @@ __global__ void __launch_bounds__(512, 2) quant_w_kernel(const float4* __restric
         const float s = __fdiv_rn(amax, 448.0f);
         const GroupScale gs(s);
         uint32_t code[8];
-#pragma unroll
         with_mode(gs, [&](auto md) {
             constexpr int kM = decltype(md)::value;
 #pragma unroll
@@ -381,7 +462,7 @@ cudaError_t launch_quant_act_rows(const void* x, int64_t rows, int64_t cols, uin
     (void)num_sms;
     const dim3 grid(static_cast<unsigned>((rows + kRowsPerCta - 1) / kRowsPerCta), static_cast<unsigned>(cols / kGroup));
     quant_act_rows_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint4*>(x), rows, cols,
-                                                    reinterpret_cast<uint2*>(q), scales);
+                                                    reinterpret_cast<uint4*>(q), scales);
     return cudaPeekAtLastError();
 }
 
@@ -389,8 +470,7 @@ cudaError_t launch_quant_act_cols(const void* x, int64_t rows, int64_t cols, uin
                                   cudaStream_t stream) {
     if (cols % kGroup == 0 && cols / kGroup <= 65535) {
         const dim3 grid(static_cast<unsigned>(rows / kGroup), static_cast<unsigned>(cols / kGroup));
-        quant_act_dual_kernel<false><<<grid, 256, 0, stream>>>(static_cast<const uint4*>(x), rows, cols, nullptr,
-                                                               nullptr, q, scales);
+        quant_act_cols_tile_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint4*>(x), rows, cols, q, scales);
         return cudaPeekAtLastError();
     }
     const int64_t tiles = (rows / kGroup) * ((cols + kColTileC - 1) / kColTileC);
@@ -404,8 +484,8 @@ cudaError_t launch_quant_act_cols(const void* x, int64_t rows, int64_t cols, uin
 cudaError_t launch_quant_act_dual(const void* x, int64_t rows, int64_t cols, uint8_t* q_row, float* s_row,
                                   uint8_t* q_col_t, float* s_col, cudaStream_t stream) {
     const dim3 grid(static_cast<unsigned>(rows / kGroup), static_cast<unsigned>(cols / kGroup));
-    quant_act_dual_kernel<true><<<grid, 256, 0, stream>>>(static_cast<const uint4*>(x), rows, cols,
-                                                          reinterpret_cast<uint2*>(q_row), s_row, q_col_t, s_col);
+    quant_act_dual_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint4*>(x), rows, cols,
+                                                          reinterpret_cast<uint4*>(q_row), s_row, q_col_t, s_col);
     return cudaPeekAtLastError();
 }
 
