@@ -283,6 +283,30 @@ def timed_rounds(kernels, rounds: int, stream):
     return per, ev[0][0].elapsed_time(ev[-1][-1])
 
 
+def b2b_ms(fn, stream, seconds: float, warmup: int = 3) -> float:
+    """Mean ms per launch of `fn(i)` launched back to back (no event between
+    launches) for at least `seconds` of GPU time; the caller rotates inputs
+    over more than twice the L2 (or uses inputs larger than L2), so that no
+    launch finds its input in L2."""
+    import torch
+    for i in range(warmup):
+        fn(i)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(5):
+        fn(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    n = int(min(20000, max(20, math.ceil(seconds * 1e3 / max(e0.elapsed_time(e1) / 5, 1e-3)))))
+    e0.record(stream)
+    for i in range(n):
+        fn(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / n
+
+
 class L2Flush:
     """Reads a buffer of 3x the L2 capacity (a reduction, no writes): the L2
     then holds only clean lines of it, so the kernel timed next starts with
@@ -533,6 +557,9 @@ def measure_config(name: str, dev, stream, pk: Peaks, seconds: float, warmup: in
             rec[kname] = pk.quant(nb, t)
             if ta is not None:
                 rec[kname]["alone"] = pk.quant(nb, ta)
+            if sets > 1 or name == "grouped":
+                fn = dict(kernels)[kname]
+                rec[kname]["b2b"] = pk.quant(nb, b2b_ms(fn, stream, min(seconds, 0.3)))
     rec["step"] = {"ms": sum(per), "TFLOP/s": flops / (sum(per) * 1e-3) / 1e12, "rounds": rounds,
                    "block_ms": block_ms, "input_sets": sets,
                    "l2": "inputs rotate over sets totalling > 2x L2" if sets > 1 else
@@ -590,6 +617,7 @@ def measure_dual(dev, stream, pk: Peaks, seconds: float):
             per, _ = timed_rounds(kern, rounds, stream)
         r = pk.quant(rows * cols * DUAL_B_PER_ELT, per[0])
         r.update({"rounds": rounds, "input_sets": sets, "clocks": clk.summary()})
+        r["b2b"] = pk.quant(rows * cols * DUAL_B_PER_ELT, b2b_ms(kern[0][1], stream, min(seconds, 0.3)))
         out[f"quant_act_dual_1x128_128x1 X[{rows},{cols}]"] = r
         del xs, base
     if fb.fp8fg_last_device_status() != 0:
@@ -782,6 +810,14 @@ def run_gpu(args):
         f["quant_act_1x128 X[4096,7168]"]["alone"] = pk.quant(ACT_BYTES, ta)
         f["quant_w_128x128 W[18432,7168]"]["alone"] = pk.quant(W_BYTES, tw)
         f["gemm_blockscaled fprop 4096x18432x7168 bf16"]["alone"] = pk.gemm(FLOPS, tg)
+        # back to back: X rotated over more than twice the L2; W alone is larger than L2
+        xsets = rotations(M * K * 2)
+        xs = [x.clone() for _ in range(xsets)]
+        f["quant_act_1x128 X[4096,7168]"]["b2b"] = pk.quant(ACT_BYTES, b2b_ms(
+            lambda i: fb.fp8_quant_act_1x128(xs[i % xsets], q=qx, scales=sx, stream=stream), stream, 0.3))
+        f["quant_w_128x128 W[18432,7168]"]["b2b"] = pk.quant(W_BYTES, b2b_ms(
+            lambda i: fb.fp8_quant_w_128x128(w, q=qw, scales=sw, stream=stream), stream, 0.3))
+        del xs
         del x_h, w_h, y_h, yhs
         torch.cuda.empty_cache()
         kernels.update(measure_dual(dev, stream, pk, args.block_seconds))

@@ -376,7 +376,11 @@ __global__ void __launch_bounds__(512, 2) quant_w_kernel(const float4* __restric
                                                       uint32_t* __restrict__ q, uint8_t* __restrict__ q_t,
                                                       float* __restrict__ scales) {
     __shared__ float red[16];
-    __shared__ uint32_t tq[kGroup][kGroup / 4 + 1];
+    // transposed tile: word w of row c (the block's column c, rows 4w..4w+3)
+    // at tq[c][w ^ (c / 4)]: the stores below (lane l writes rows 4l..4l+3 of
+    // one word column) and the loads (a warp reads 8 rows whose c / 4 are
+    // distinct) then touch 32 distinct banks per instruction
+    __shared__ uint32_t tq[kGroup][kGroup / 4];
     const int t = threadIdx.x, lane = t & 31, wid = t >> 5;
     const int64_t nbr = rows / kGroup, nbc = cols / kGroup;
     for (int64_t blk = blockIdx.x; blk < nbr * nbc; blk += gridDim.x) {
@@ -429,24 +433,28 @@ __global__ void __launch_bounds__(512, 2) quant_w_kernel(const float4* __restric
                 const uint32_t c1w = __byte_perm(lo01, lo23, 0x7632);
                 const uint32_t c2w = __byte_perm(hi01, hi23, 0x5410);
                 const uint32_t c3w = __byte_perm(hi01, hi23, 0x7632);
-                const int rw = 16 * h + wid;  // word index along rows: rows 4*rw .. 4*rw+3
+                const int rw = (16 * h + wid) ^ lane;  // word along rows (rows 4(16h+wid)..+3), swizzled
                 tq[4 * lane + 0][rw] = c0w;
                 tq[4 * lane + 1][rw] = c1w;
                 tq[4 * lane + 2][rw] = c2w;
                 tq[4 * lane + 3][rw] = c3w;
             }
             __syncthreads();
-            // q_t row (c0 + j) receives the block's column j: 128 bytes = 32 words
-            const int j = t >> 2, part = t & 3;
+            // q_t row (c0 + j) receives the block's column j: 128 bytes = 32
+            // words, a quarter (part) per thread; a warp covers the 8 rows
+            // j = 32 (wid % 4) + 4 b + wid / 4 (b < 8), whose j / 4 differ
+            const int part = lane & 3;
+            const int j = 32 * (wid & 3) + 4 * (lane >> 2) + (wid >> 2);
+            const int sw = j >> 2;
             uint4 o0, o1;
-            o0.x = tq[j][8 * part + 0];
-            o0.y = tq[j][8 * part + 1];
-            o0.z = tq[j][8 * part + 2];
-            o0.w = tq[j][8 * part + 3];
-            o1.x = tq[j][8 * part + 4];
-            o1.y = tq[j][8 * part + 5];
-            o1.z = tq[j][8 * part + 6];
-            o1.w = tq[j][8 * part + 7];
+            o0.x = tq[j][(8 * part + 0) ^ sw];
+            o0.y = tq[j][(8 * part + 1) ^ sw];
+            o0.z = tq[j][(8 * part + 2) ^ sw];
+            o0.w = tq[j][(8 * part + 3) ^ sw];
+            o1.x = tq[j][(8 * part + 4) ^ sw];
+            o1.y = tq[j][(8 * part + 5) ^ sw];
+            o1.z = tq[j][(8 * part + 6) ^ sw];
+            o1.w = tq[j][(8 * part + 7) ^ sw];
             uint4* dst = reinterpret_cast<uint4*>(q_t + (c0 + j) * rows + r0 + 32 * part);
             __stcs(dst, o0);
             __stcs(dst + 1, o1);
