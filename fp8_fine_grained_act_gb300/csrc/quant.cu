@@ -241,9 +241,12 @@ __global__ void __launch_bounds__(256, 4) quant_act_dual_kernel(const uint4* __r
     __syncthreads();
     const int cp = t & 63;   // channel pair: channels 2cp, 2cp+1 of the tile
     const int rs = t >> 6;   // token segment: tokens 32rs .. 32rs+31
+    uint32_t w[32];          // the segment's words, read once for the maximum and the codes
+#pragma unroll
+    for (int r = 0; r < 32; ++r) w[r] = tile[32 * rs + r][cp];
     uint32_t m2 = 0;         // both channels' maxima as 16-bit patterns
 #pragma unroll
-    for (int r = 0; r < 32; ++r) m2 = __vmaxu2(m2, tile[32 * rs + r][cp] & 0x7FFF7FFFu);
+    for (int r = 0; r < 32; ++r) m2 = __vmaxu2(m2, w[r] & 0x7FFF7FFFu);
     part[rs][2 * cp] = __uint_as_float(m2 << 16);
     part[rs][2 * cp + 1] = __uint_as_float(m2 & 0xFFFF0000u);
     __syncthreads();
@@ -260,26 +263,24 @@ __global__ void __launch_bounds__(256, 4) quant_act_dual_kernel(const uint4* __r
     uint4* dst1 = reinterpret_cast<uint4*>(q_col_t + (ch0 + 1) * rows + r0 + 32 * rs);
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
-        uint32_t w[16];
-#pragma unroll
-        for (int r = 0; r < 16; ++r) w[r] = tile[32 * rs + 16 * k + r][cp];
+        const uint32_t* wk = w + 16 * k;
         // channel 2cp: the low halves of four consecutive tokens' words
         with_mode(g0, [&](auto md) {
             constexpr int kM = decltype(md)::value;
             uint4 o;
-            o.x = quant_quad<kM>(bf16_lo(w[0]), bf16_lo(w[1]), bf16_lo(w[2]), bf16_lo(w[3]), g0);
-            o.y = quant_quad<kM>(bf16_lo(w[4]), bf16_lo(w[5]), bf16_lo(w[6]), bf16_lo(w[7]), g0);
-            o.z = quant_quad<kM>(bf16_lo(w[8]), bf16_lo(w[9]), bf16_lo(w[10]), bf16_lo(w[11]), g0);
-            o.w = quant_quad<kM>(bf16_lo(w[12]), bf16_lo(w[13]), bf16_lo(w[14]), bf16_lo(w[15]), g0);
+            o.x = quant_quad<kM>(bf16_lo(wk[0]), bf16_lo(wk[1]), bf16_lo(wk[2]), bf16_lo(wk[3]), g0);
+            o.y = quant_quad<kM>(bf16_lo(wk[4]), bf16_lo(wk[5]), bf16_lo(wk[6]), bf16_lo(wk[7]), g0);
+            o.z = quant_quad<kM>(bf16_lo(wk[8]), bf16_lo(wk[9]), bf16_lo(wk[10]), bf16_lo(wk[11]), g0);
+            o.w = quant_quad<kM>(bf16_lo(wk[12]), bf16_lo(wk[13]), bf16_lo(wk[14]), bf16_lo(wk[15]), g0);
             __stcs(dst0 + k, o);
         });
         with_mode(g1, [&](auto md) {
             constexpr int kM = decltype(md)::value;
             uint4 o;
-            o.x = quant_quad<kM>(bf16_hi(w[0]), bf16_hi(w[1]), bf16_hi(w[2]), bf16_hi(w[3]), g1);
-            o.y = quant_quad<kM>(bf16_hi(w[4]), bf16_hi(w[5]), bf16_hi(w[6]), bf16_hi(w[7]), g1);
-            o.z = quant_quad<kM>(bf16_hi(w[8]), bf16_hi(w[9]), bf16_hi(w[10]), bf16_hi(w[11]), g1);
-            o.w = quant_quad<kM>(bf16_hi(w[12]), bf16_hi(w[13]), bf16_hi(w[14]), bf16_hi(w[15]), g1);
+            o.x = quant_quad<kM>(bf16_hi(wk[0]), bf16_hi(wk[1]), bf16_hi(wk[2]), bf16_hi(wk[3]), g1);
+            o.y = quant_quad<kM>(bf16_hi(wk[4]), bf16_hi(wk[5]), bf16_hi(wk[6]), bf16_hi(wk[7]), g1);
+            o.z = quant_quad<kM>(bf16_hi(wk[8]), bf16_hi(wk[9]), bf16_hi(wk[10]), bf16_hi(wk[11]), g1);
+            o.w = quant_quad<kM>(bf16_hi(wk[12]), bf16_hi(wk[13]), bf16_hi(wk[14]), bf16_hi(wk[15]), g1);
             __stcs(dst1 + k, o);
         });
     }
