@@ -736,7 +736,8 @@ FP8FG_DEV void run_epilogue_rowb(Smem<1>& sm, uint32_t tmem_base, const Params& 
 // 32 KB slots laid over the GEMM's idle operand stages and output staging; the 256 threads of
 // warps 4-11 quantize each tile from shared memory with
 // fp8_quant_act_1x128's mapping and arithmetic (a lane quad per row group,
-// lane j holding chunks j, j+4, j+8, j+12; two rows per thread), so the codes
+// lane j holding chunks 2j, 2j+1, 2j+8, 2j+9, written as two 16-byte runs;
+// two rows per thread), so the codes
 // and scales are the ones that quantizer writes; once the CTA's share is
 // done, each of its tiles is added to its band's counter with a release at
 // GPU scope.  Sources: DeepSeek-V3 FP8 post
@@ -784,7 +785,7 @@ FP8FG_DEV uint32_t p1_load(Smem<kRowB>& sm, const CUtensorMap* tmap_x, const Par
 template <int kRowB>
 FP8FG_DEV bool p1_quantize(Smem<kRowB>& sm, const Params& p, int64_t units, int64_t kb, int tid) {
     volatile int* abort_flag = &sm.abort_flag;
-    const int j = tid & 3;     // chunks j, j+4, j+8, j+12 of the row group
+    const int j = tid & 3;     // chunks 2j, 2j+1, 2j+8, 2j+9 of the row group
     const int rq = tid >> 2;   // row within a 64-row half of the tile
     const int lane = tid & 31;
     bool ok = true;            // warp-uniform
@@ -800,29 +801,39 @@ FP8FG_DEV bool p1_quantize(Smem<kRowB>& sm, const Params& p, int64_t units, int6
             const uint32_t m = static_cast<uint32_t>(t) / static_cast<uint32_t>(kb);
             const uint32_t c = static_cast<uint32_t>(t) - m * static_cast<uint32_t>(kb);
             const uint32_t slot = p1_slot(sm, i);
+            // both rows' chunks first (eight loads in flight), then the groups
+            uint4 v[2][4];
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
                 const int r = rq + 64 * u;
-                uint4 v[4];
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
-                    // chunk j + 4k of the row: box k / 2, 16-byte unit j + 4 (k & 1), 128-byte swizzle
-                    const uint32_t unit = static_cast<uint32_t>(j + 4 * (k & 1)) ^ static_cast<uint32_t>(r & 7);
-                    v[k] = ld_shared_v4(slot + (k >> 1) * kP1BoxBytes + r * 128 + (unit << 4));
+                    // chunk 2j + (k & 1) + 8 (k / 2) of the row: box k / 2, 16-byte unit
+                    // 2j + (k & 1) of its 128-byte row, 128-byte swizzle (the two rows of
+                    // a quarter-warp then read disjoint banks)
+                    const uint32_t unit = static_cast<uint32_t>(2 * j + (k & 1)) ^ static_cast<uint32_t>(r & 7);
+                    v[u][k] = ld_shared_v4(slot + (k >> 1) * kP1BoxBytes + r * 128 + (unit << 4));
                 }
-                const float amax = quad_amax_bf16(v);
+            }
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int r = rq + 64 * u;
+                const float amax = quad_amax_bf16(v[u]);
                 const float s = __fdiv_rn(amax, 448.0f);
                 const GroupScale gs(s);
                 const int64_t row = static_cast<int64_t>(m) * BM + r;
-                uint2* dst = p.qa + (row * p.K + static_cast<int64_t>(c) * BK) / 8 + j;
+                // codes of chunks 2j, 2j+1 and of chunks 2j+8, 2j+9: two 16-byte stores
+                uint4* dst = reinterpret_cast<uint4*>(p.qa) + (row * p.K + static_cast<int64_t>(c) * BK) / 16 + j;
                 with_mode(gs, [&](auto md) {
                     constexpr int kM = decltype(md)::value;
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        uint2 out;
-                        out.x = quant_quad_bf16<kM>(v[k].x, v[k].y, gs);
-                        out.y = quant_quad_bf16<kM>(v[k].z, v[k].w, gs);
-                        __stcs(dst + 4 * k, out);
+                    for (int h = 0; h < 2; ++h) {
+                        uint4 out;
+                        out.x = quant_quad_bf16<kM>(v[u][2 * h].x, v[u][2 * h].y, gs);
+                        out.y = quant_quad_bf16<kM>(v[u][2 * h].z, v[u][2 * h].w, gs);
+                        out.z = quant_quad_bf16<kM>(v[u][2 * h + 1].x, v[u][2 * h + 1].y, gs);
+                        out.w = quant_quad_bf16<kM>(v[u][2 * h + 1].z, v[u][2 * h + 1].w, gs);
+                        __stcs(dst + 4 * h, out);
                     }
                 });
                 if (j == 0) p.sa_out[static_cast<int64_t>(c) * p.M + row] = s;
