@@ -39,7 +39,7 @@ std::mutex g_dev_mu;
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 // Scale arrays are read and written one float at a time (except the GEMM's
-// per-row B scales, which arrive by bulk copies): 4-byte alignment suffices.
+// per-row B scales, read in 8-byte pairs): 4-byte alignment suffices.
 bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
 // Probe the current device once; returns a library status.
@@ -163,7 +163,7 @@ int fp8_gemm_blockscaled(const uint8_t* a, const float* sa, const uint8_t* b, co
     if (M == 0 || N == 0) return kOk;
     if (!d) return kErrInvalidArg;
     if (K > 0 && (!a || !sa || !b || !sb)) return kErrInvalidArg;
-    // per-row B scales: both scale arrays arrive by 16-byte bulk copies
+    // per-row B scales: both scale arrays 16-byte aligned (B scales are read in 8-byte pairs)
     const bool row = bscale == FP8FG_BSCALE_ROW;
     const bool sa_ok = row ? aligned16(sa) : aligned4(sa);
     const bool sb_ok = row ? aligned16(sb) : aligned4(sb);

@@ -228,20 +228,19 @@ FP8FG_DEV uint32_t pack_bf16x2(float lo, float hi) {
 }
 
 // ------------------------------------------------------------ producer ---
-// kRowB: B scales per row of B per K chunk (1) or per 128x128 block (0).
+// One thread: the A and B operand tiles of every chunk, by TMA.
 template <int kRowB>
 FP8FG_DEV void run_producer(Smem<kRowB>& sm, const CUtensorMap* tmap_a, const CUtensorMap* tmap_b, const Params& p,
                             int64_t m_tiles, int64_t n_tiles, int64_t kb) {
-    constexpr int ST = Smem<kRowB>::kStages, SL = Smem<kRowB>::kSlots;
+    constexpr int ST = Smem<kRowB>::kStages;
     volatile int* abort_flag = &sm.abort_flag;
-    uint32_t g_ab = 0, g_sc = 0;  // chunks whose operand / scale copies were issued
+    uint32_t g_ab = 0;  // chunks whose operand copies were issued
     const int64_t num_tiles = m_tiles * n_tiles;
     bool ok = true;
     for (int64_t t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
         int64_t m0, n0;
         tile_origin(t, m_tiles, n_tiles, p.m_fastest, m0, n0);
         const int e = p.offsets ? expert_of(p.offsets, p.G, m0) : 0;
-        const uint32_t sc_bytes = static_cast<uint32_t>(min(static_cast<int64_t>(BN), p.N - n0) * 4);
         for (int64_t c = 0; c < kb; ++c) {
             const uint32_t s = g_ab % ST;
             if (g_ab >= static_cast<uint32_t>(ST)) {
@@ -270,18 +269,6 @@ FP8FG_DEV void run_producer(Smem<kRowB>& sm, const CUtensorMap* tmap_a, const CU
             else
                 tma_load_2d(smem_u32(sm.b[s]), tmap_b, static_cast<int32_t>(c * BK), static_cast<int32_t>(n0), fb);
             ++g_ab;
-            if (!kRowB) continue;
-            const uint32_t sl = g_sc % SL, sph = (g_sc / SL) & 1;
-            if (!mbar_wait_bounded(smem_u32(&sm.sempty[sl]), sph ^ 1, abort_flag, p.status, p.limit_ns,
-                                   kErrTimeout)) {
-                ok = false;
-                break;
-            }
-            const uint32_t sfb = smem_u32(&sm.sfull[sl]);
-            mbar_arrive_expect_tx(sfb, sc_bytes + BM * 4);
-            bulk_load(smem_u32(sm.sb[sl]), p.sb + c * p.N + n0, sc_bytes, sfb);
-            bulk_load(smem_u32(sm.sa[sl]), p.sa + c * p.M + m0, BM * 4, sfb);
-            ++g_sc;
         }
     }
     if (!ok) {
@@ -293,11 +280,67 @@ FP8FG_DEV void run_producer(Smem<kRowB>& sm, const CUtensorMap* tmap_a, const CU
             const uint32_t last = s + ST * ((g_ab - 1 - s) / ST);
             landed &= wait_plain(smem_u32(&sm.full[s]), (last / ST) & 1, kTeardownLimitNs);
         }
-        for (uint32_t s = 0; s < SL && s < g_sc; ++s) {
-            const uint32_t last = s + SL * ((g_sc - 1 - s) / SL);
-            landed &= wait_plain(smem_u32(&sm.sfull[s]), (last / SL) & 1, kTeardownLimitNs);
-        }
         if (!landed) atomicExch(p.status, kErrTeardown);
+    }
+}
+
+// ---------------------------------------------- per-row scale stager ---
+// Per-row B scales only; warp 3.  For every chunk, in the MMA warp's order:
+// load the chunk's B scales of the tile's 256 columns and A scales of its
+// 128 rows from global memory, wait until the promotion warps have released
+// the ring slot, and store the scales into it permuted so that a promotion
+// thread (run_epilogue_rowb) finds its 4 A scales in one 16-byte run and the
+// B scales of each 32 of its columns in two.  Every lane then arrives on the
+// slot's "full" barrier (count 32).  Layouts of a slot:
+//   B: position 128 h + 32 s + 16 p + 4 q + 2 b + e holds column
+//      128 h + 32 s + 8 (2 p + b) + 2 q + e of the tile;
+//   A: position 32 u + 4 r + k holds row 32 u + r + 8 k.
+// Lane l stores positions 4 l .. 4 l + 3 of A and of each half h of B, so
+// each store instruction writes 512 contiguous bytes.  The scales are not
+// copied by TMA because the permutation has 8-byte granularity; doing it
+// here keeps the promotion warps' shared loads (which compete with the
+// tensor core's operand reads) at 9 per chunk instead of 20.
+FP8FG_DEV void run_scales(Smem<1>& sm, const Params& p, int64_t m_tiles, int64_t n_tiles, int64_t kb, int lane) {
+    constexpr int SL = Smem<1>::kSlots;
+    volatile int* abort_flag = &sm.abort_flag;
+    const int64_t num_tiles = m_tiles * n_tiles;
+    // this lane's B columns cb, cb + 1, cb + 8, cb + 9 (and + 128), A rows ra + 8 k
+    const int cb = 32 * (lane >> 3) + 16 * ((lane >> 2) & 1) + 2 * (lane & 3);
+    const int ra = 32 * (lane >> 3) + (lane & 7);
+    uint32_t g = 0;
+    for (int64_t t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+        int64_t m0, n0;
+        tile_origin(t, m_tiles, n_tiles, p.m_fastest, m0, n0);
+        const bool hi = n0 + 128 < p.N;   // the tile's second 128 columns exist (N is a multiple of 128)
+        for (int64_t c = 0; c < kb; ++c, ++g) {
+            const uint32_t sl = g % SL, sph = (g / SL) & 1;
+            // the loads go out before the wait for the slot
+            const float* sbr = p.sb + c * p.N + n0 + cb;
+            const float* sar = p.sa + c * p.M + m0 + ra;
+            const float2 b0 = __ldg(reinterpret_cast<const float2*>(sbr));
+            const float2 b1 = __ldg(reinterpret_cast<const float2*>(sbr + 8));
+            float2 b2 = make_float2(0.0f, 0.0f), b3 = make_float2(0.0f, 0.0f);
+            if (hi) {
+                b2 = __ldg(reinterpret_cast<const float2*>(sbr + 128));
+                b3 = __ldg(reinterpret_cast<const float2*>(sbr + 136));
+            }
+            float a[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) a[k] = __ldg(sar + 8 * k);
+            bool ok = true;
+            if (lane == 0)
+                ok = mbar_wait_bounded(smem_u32(&sm.sempty[sl]), sph ^ 1, abort_flag, p.status, p.limit_ns,
+                                       kErrTimeout);
+            if (!__shfl_sync(0xffffffffu, ok, 0)) return;
+            const uint32_t sb_s = smem_u32(sm.sb[sl]) + 16 * lane, sa_s = smem_u32(sm.sa[sl]) + 16 * lane;
+            st_shared_v4(sb_s, __float_as_uint(b0.x), __float_as_uint(b0.y), __float_as_uint(b1.x),
+                         __float_as_uint(b1.y));
+            st_shared_v4(sb_s + 512, __float_as_uint(b2.x), __float_as_uint(b2.y), __float_as_uint(b3.x),
+                         __float_as_uint(b3.y));
+            st_shared_v4(sa_s, __float_as_uint(a[0]), __float_as_uint(a[1]), __float_as_uint(a[2]),
+                         __float_as_uint(a[3]));
+            mbar_arrive(smem_u32(&sm.sfull[sl]));
+        }
     }
 }
 
@@ -621,14 +664,23 @@ FP8FG_DEV void run_epilogue_rowb(Smem<1>& sm, uint32_t tmem_base, const Params& 
             tc_fence_after();
             if (active && !dead) {
                 const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + buf * BN + ECOLS * half;
-                const float* sbp = sm.sb[sl] + ECOLS * half + 2 * q;
-                const float* sap = sm.sa[sl] + quad * 32 + g4;
-                float sav[4];   // A scales of rows 8k + g: (rh, rr) = (k / 2, k % 2)
-#pragma unroll
-                for (int k = 0; k < 4; ++k) sav[k] = sap[8 * k];
+                // the slot's permuted layouts (run_scales): A rows 8k + g4 of
+                // this warp's 32 at 4 g4 + k, B columns 8 bb + 2 q + e of each
+                // 32 at 16 (bb / 2) + 4 q + 2 (bb % 2) + e
+                const uint32_t sbp = smem_u32(sm.sb[sl] + ECOLS * half + 4 * q);
+                const uint4 sa4 = ld_shared_v4(smem_u32(sm.sa[sl] + quad * 32 + 4 * g4));
+                // A scales of rows 8k + g4: (rh, rr) = (k / 2, k % 2)
+                const float sav[4] = {__uint_as_float(sa4.x), __uint_as_float(sa4.y), __uint_as_float(sa4.z),
+                                      __uint_as_float(sa4.w)};
                 float2 sbv[4];  // B scales of the current 32 columns
-#pragma unroll
-                for (int bb = 0; bb < 4; ++bb) sbv[bb] = *reinterpret_cast<const float2*>(sbp + 8 * bb);
+                auto load_sb = [&](int seg) {
+                    const uint4 lo = ld_shared_v4(sbp + 128 * seg), hi = ld_shared_v4(sbp + 128 * seg + 64);
+                    sbv[0] = make_float2(__uint_as_float(lo.x), __uint_as_float(lo.y));
+                    sbv[1] = make_float2(__uint_as_float(lo.z), __uint_as_float(lo.w));
+                    sbv[2] = make_float2(__uint_as_float(hi.x), __uint_as_float(hi.y));
+                    sbv[3] = make_float2(__uint_as_float(hi.z), __uint_as_float(hi.w));
+                };
+                load_sb(0);
                 uint32_t r[2][16];
                 tmem_ld_16x256b_x4(taddr, r[0]);
                 tmem_ld_wait(r[0]);
@@ -652,11 +704,7 @@ FP8FG_DEV void run_epilogue_rowb(Smem<1>& sm, uint32_t tmem_base, const Params& 
                         }
                     }
                     if (j + 1 < 8) {
-                        if (j & 1) {   // the next load starts the next 32 columns
-#pragma unroll
-                            for (int bb = 0; bb < 4; ++bb)
-                                sbv[bb] = *reinterpret_cast<const float2*>(sbp + 32 * ((j + 1) >> 1) + 8 * bb);
-                        }
+                        if (j & 1) load_sb((j + 1) >> 1);   // the next load starts the next 32 columns
                         tmem_ld_wait(r[(j + 1) & 1]);
                     }
                 }
@@ -891,7 +939,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int s = 0; s < S::kStages; ++s) mbar_init(smem_u32(&sm.full[s]), 1);
         for (uint32_t d = 0; d < kDone; ++d) mbar_init(smem_u32(&sm.done[d]), 1);
         for (int s = 0; s < S::kSlots; ++s) {
-            mbar_init(smem_u32(&sm.sfull[s]), 1);
+            mbar_init(smem_u32(&sm.sfull[s]), 32);   // the 32 lanes of the scale stager
             mbar_init(smem_u32(&sm.sempty[s]), EPI_WARPS);
         }
         mbar_init(smem_u32(&sm.drain), 1);
@@ -957,6 +1005,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (warp == 0 && lane == 0) run_producer<kRowB>(sm, &tmap_a, &tmap_b, p, m_tiles, n_tiles, kb);
         if (warp == 1) run_mma<kRowB>(sm, tmem_base, p, m_tiles, n_tiles, kb, lane);
         if (warp == 2) run_watch<kRowB>(sm, p, m_tiles, n_tiles, kb, lane);
+        if constexpr (kRowB != 0)
+            if (warp == 3) run_scales(sm, p, m_tiles, n_tiles, kb, lane);
     } else {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(REGS_HIGH));
         if constexpr (kRowB != 0)

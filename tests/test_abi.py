@@ -125,8 +125,8 @@ def test_gemm_argument_checks(lib):
     assert call(sn=-1) == 1
     assert call(a=None) == 1 and call(sb=None) == 1 and call(d=None) == 1
     assert call(a=MIS) == 2 and call(d=MIS) == 2 and call(sa=MIS2) == 2 and call(sb=MIS2) == 2
-    assert call(bscale=1, sb=MIS) == 2                     # per-row B scales arrive by 16-byte bulk copies
-    assert call(bscale=1, sa=MIS) == 2                     # ... and so do the A scales in that mode
+    assert call(bscale=1, sb=MIS) == 2                     # per-row B scales: 16-byte aligned scale arrays
+    assert call(bscale=1, sa=MIS) == 2                     # ... both of them
     if not _has_gpu():
         assert call(sa=MIS) in NOPROBE and call(sb=MIS) in NOPROBE
     assert call(M=0, a=None, d=None) == 0                  # empty: no-op
