@@ -227,6 +227,30 @@ def cpu_baseline(mb: int, nb: int, seed: int = 1):
     return 2.0 * mb * nb * K / dt / 1e12, oracle.num_threads(), dt
 
 
+def cpu_quantizers_1core(rows: int, seed: int = 1):
+    """The oracle's two Fprop quantizers on one host core (the all-core
+    figure is the GEMM-dominated cpu_baseline value): X[rows, K] 1x128 and
+    W[rows, K] 128x128, as algorithmic GB/s.  The thread count is restored."""
+    import oracle
+    from fp8_fine_grained_act_gb300 import synth
+    d = synth.fprop_linear(seed=seed, M=rows, N=rows, K=K)
+    n0 = oracle.num_threads()
+    oracle.set_num_threads(1)
+    try:
+        t0 = time.perf_counter()
+        oracle.quant_act(d["x"])
+        t1 = time.perf_counter()
+        oracle.quant_w(d["w"])
+        t2 = time.perf_counter()
+    finally:
+        oracle.set_num_threads(n0)
+    act_b = rows * K * (2 + 1 + 4 / 128)
+    w_b = rows * K * (4 + 1 + 4 / 16384)
+    return {"cores": 1,
+            "quant_act_1x128": {"GB/s": act_b / (t1 - t0) / 1e9, "sample": f"X[{rows},{K}] bf16", "s": t1 - t0},
+            "quant_w_128x128": {"GB/s": w_b / (t2 - t1) / 1e9, "sample": f"W[{rows},{K}] fp32", "s": t2 - t1}}
+
+
 def run_reference(args):
     """The oracle arm: each step is a bounded sample of the workload, sized
     so that warm-up plus timed steps take about two minutes."""
@@ -876,7 +900,8 @@ def run_gpu(args):
         v, cores, dt = cpu_baseline(mb, nb)
         line["cpu_baseline"] = {"value": v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                                 "sample": f"first {mb} tokens x {nb} output channels of the workload: both "
-                                          f"quantizers + {mb}x{nb}x{K} double GEMM, {dt:.1f} s"}
+                                          f"quantizers + {mb}x{nb}x{K} double GEMM, {dt:.1f} s",
+                                "quantizers_1core": cpu_quantizers_1core(1024)}
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()

@@ -2,7 +2,8 @@
 committed ncu summary to the kernel it was taken on, and the lookup of the
 summary's DRAM traffic.  A comment-only edit must keep the hash (the summary
 still describes the same code); any code edit must change it (the traffic is
-then reported as null rather than attributed to a different kernel)."""
+then reported as null rather than attributed to a different kernel).  Also
+the single-core timing of the oracle's quantizers."""
 from __future__ import annotations
 
 import os
@@ -58,3 +59,14 @@ def test_committed_summary_names_a_hash_and_traffic():
                              "gemm_blockscaled_fprop_4096x18432x7168.md")).read()
     assert "kernel source sha256[:16]:" in text
     assert "dram bytes per launch (read + write):" in text
+
+
+def test_single_core_quantizer_timing_restores_threads():
+    """The oracle's quantizers timed on one core report positive rates and
+    leave the oracle's thread count as it was."""
+    import oracle
+    n0 = oracle.num_threads()
+    r = bench.cpu_quantizers_1core(128)
+    assert r["cores"] == 1
+    assert r["quant_act_1x128"]["GB/s"] > 0 and r["quant_w_128x128"]["GB/s"] > 0
+    assert oracle.num_threads() == n0
