@@ -907,21 +907,30 @@ FP8FG_DEV bool p1_quantize(Smem<kRowB>& sm, const Params& p, int64_t units, int6
     return ok;
 }
 
-// Thread 0 of every CTA: wait until every band's kb tiles are published
-// (acquire), bounded by the wait limit; a timeout records
-// FP8FG_ERR_TIMEOUT and the CTA computes nothing.
-FP8FG_DEV bool wait_bands(const Params& p, int64_t m_tiles, int64_t kb) {
+// Warp 0 of every CTA: wait until every band's kb tiles are published
+// (acquire), lane l polling bands l, l + 32, ... (in parallel: one polling
+// thread reading the counters one after another took several microseconds
+// more), each lane bounded by the wait limit.  Returns the same verdict in
+// every lane; a timeout records FP8FG_ERR_TIMEOUT and the CTA computes
+// nothing.
+FP8FG_DEV bool wait_bands(const Params& p, int64_t m_tiles, int64_t kb, int lane) {
     const uint64_t t0 = globaltimer_ns();
-    for (int64_t m = 0; m < m_tiles; ++m) {
+    bool ok = true;
+    for (int64_t m = lane; ok && m < m_tiles; m += 32) {
         while (ld_acquire_gpu(p.band_flags + m) < kb) {
             if (globaltimer_ns() - t0 > p.limit_ns) {
-                atomicCAS(p.status, 0, kErrTimeout);
-                return false;
+                ok = false;
+                break;
             }
         }
     }
-    fence_proxy_async_global();   // before this thread (the producer) issues TMA reads of q_a
-    return true;
+    __syncwarp();   // every lane's acquires before lane 0's TMA reads of q_a
+    ok = __all_sync(0xffffffffu, ok);
+    if (lane == 0) {
+        if (!ok) atomicCAS(p.status, 0, kErrTimeout);
+        fence_proxy_async_global();   // before this thread (the producer) issues TMA reads of q_a
+    }
+    return ok;
 }
 
 template <int kRowB, bool kFusedA>
@@ -975,10 +984,12 @@ __global__ void __launch_bounds__(THREADS, 1)
         // phase 1 (all CTAs are resident: cooperative launch): quantize this
         // CTA's share of A, then wait for every CTA's share
         const int64_t units = m_tiles * kb;
-        if (threadIdx.x == 0) {
-            const uint32_t issued = p1_load(sm, &tmap_x, p, units, kb);
-            if (!wait_bands(p, m_tiles, kb)) stop = 1;
-            if (stop || *static_cast<volatile int*>(&sm.abort_flag)) {
+        if (warp == 0) {
+            uint32_t issued = 0;
+            if (lane == 0) issued = p1_load(sm, &tmap_x, p, units, kb);
+            __syncwarp();
+            if (!wait_bands(p, m_tiles, kb, lane)) stop = 1;
+            if (lane == 0 && (stop || *static_cast<volatile int*>(&sm.abort_flag))) {
                 // let every copy issued into the ring land before the stages are reused or released
                 bool landed = true;
                 for (uint32_t s = 0; s < kP1Slots && s < issued; ++s) {
