@@ -1,7 +1,8 @@
 """Bounded device waits: a kernel whose mbarrier is never signalled gives up
 after its limit, records FP8FG_ERR_TIMEOUT in the device status word and
-returns; the context stays usable.  The GEMM's own waits are made to run out
-with a 1 ns limit.  No fault, trap or hang is involved."""
+returns; the context stays usable.  The GEMM's own waits, and those of the
+fused quantizer + GEMM, are made to run out with a 1 ns limit.  No fault,
+trap or hang is involved."""
 from __future__ import annotations
 
 import time
@@ -13,7 +14,7 @@ import torch
 import oracle
 from fp8_fine_grained_act_gb300 import binding as fb
 from fp8_fine_grained_act_gb300 import synth
-from gpu_util import dev_bf16, host
+from gpu_util import dev, dev_bf16, host
 
 pytestmark = pytest.mark.gpu
 
@@ -63,3 +64,32 @@ def test_gemm_waits_run_out_and_the_kernel_ends(gpu_device, bscale):
     o, m = oracle.gemm_entries(host(a), host(sa), host(b), host(sb), ii, jj,
                                bscale=oracle.BSCALE_BLOCK128 if bscale == fb.FP8FG_BSCALE_BLOCK128 else oracle.BSCALE_ROW)
     assert np.all(np.abs(host(d)[ii, jj] - o) <= oracle.gemm_tolerance(o, m, "f32"))
+
+
+def test_fused_quantizer_waits_run_out_and_the_kernel_ends(gpu_device):
+    """fp8_gemm_quant_a with a 1 ns limit: the phase-1 ring's waits and the
+    band waits (each lane of warp 0 polling its own band counters) give up,
+    every CTA ends without computing, FP8FG_ERR_TIMEOUT is reported, and the
+    next call with the default limit equals the two-launch path (quantizer,
+    then GEMM) bit for bit."""
+    d = synth.fprop_linear(seed=21, M=1024, N=512, K=1024)
+    x = dev_bf16(d["x"], gpu_device)
+    qw, sw = fb.fp8_quant_w_128x128(dev(d["w"], gpu_device))
+    torch.cuda.synchronize()
+    fb.fp8fg_last_device_status()                            # clear
+    assert fb.fp8fg_set_wait_limit(1) == 0
+    try:
+        t0 = time.perf_counter()
+        fb.fp8_gemm_quant_a(x, qw, sw, out_dtype=fb.FP8FG_OUT_F32)
+        st = fb.fp8fg_last_device_status()
+        assert time.perf_counter() - t0 < 30.0
+    finally:
+        assert fb.fp8fg_set_wait_limit(0) == 0
+    assert st == fb.FP8FG_ERR_TIMEOUT
+    y, q_a, s_a = fb.fp8_gemm_quant_a(x, qw, sw, out_dtype=fb.FP8FG_OUT_F32)
+    qa_ref, sa_ref = fb.fp8_quant_act_1x128(x)
+    y_ref = fb.fp8_gemm_blockscaled(qa_ref, sa_ref, qw, sw, out_dtype=fb.FP8FG_OUT_F32)
+    torch.cuda.synchronize()
+    assert fb.fp8fg_last_device_status() == 0
+    assert torch.equal(q_a, qa_ref) and torch.equal(s_a, sa_ref)
+    assert torch.equal(y.view(torch.int32), y_ref.view(torch.int32))
