@@ -14,7 +14,9 @@ comes from its own maximum).  Two sweeps cover that dependence:
   saturate; normal; subnormal; the tie to zero), under block scales with random
   mantissas, all-ones mantissas and scales on both sides of 2^-90 (below
   which the kernel switches from the corrected reciprocal to a full
-  division).
+  division);
+* the conversion alone: every finite FP32 value of magnitude at most 448,
+  both signs, encoded under a block scale of exactly 1.
 """
 from __future__ import annotations
 
@@ -118,3 +120,36 @@ def test_weight_path_every_fp32_mantissa(gpu_device, amax_bits):
     w = np.ascontiguousarray(blocks.reshape(nb, 128, 128).transpose(1, 0, 2).reshape(128, nb * 128))
     for c0 in range(0, nb, 1024):                  # at most 1024 blocks (16.8M elements) per round
         _weight_parity(np.ascontiguousarray(w[:, c0 * 128:(c0 + 1024) * 128]), gpu_device)
+
+
+def test_encoder_every_fp32_value_up_to_448(gpu_device):
+    """The GPU's FP32 -> E4M3 conversion on every finite FP32 pattern of
+    magnitude at most 448, both signs (2.28e9 values), against the oracle's
+    encoder.  Each 128x128 block of the weight quantizer's input holds 448
+    in its first element and test values elsewhere, so its scale is
+    fl32(448 / 448) = 1 and every code is the encoding of fl32(x / 1) = x
+    itself: the conversion is checked alone, with no scale in between."""
+    top = np.uint32(0x43E00000)                  # 448.0f
+    per_block = 128 * 128 - 1
+    step = per_block * 2048                      # values per round (~2^25)
+    total = 0
+    for start in range(0, int(top) + 1, step):
+        bits = np.arange(start, min(start + step, int(top) + 1), dtype=np.uint32)
+        ref = oracle.e4m3_encode(bits.view(np.float32))
+        nb = -(-len(bits) // per_block)
+        for sign in (np.uint32(0), np.uint32(0x80000000)):
+            vals = np.zeros(nb * per_block, np.uint32)
+            vals[:len(bits)] = bits | sign
+            w = np.empty((nb, per_block + 1), np.float32)
+            w[:, 0] = 448.0
+            w[:, 1:] = vals.reshape(nb, per_block).view(np.float32)
+            q, s = fb.fp8_quant_w_128x128(dev(w.reshape(nb * 128, 128), gpu_device))
+            torch.cuda.synchronize()
+            assert np.all(host(s) == 1.0)
+            qg = host(q).reshape(nb, per_block + 1)[:, 1:].reshape(-1)[:len(bits)]
+            want = ref | np.uint8(0x80) if sign else ref
+            bad = np.flatnonzero(qg != want)
+            assert len(bad) == 0, f"{len(bad)} codes differ, first x=0x{int(bits[bad[0]] | sign):08x} " \
+                                  f"gpu=0x{qg[bad[0]]:02x} oracle=0x{want[bad[0]]:02x}"
+            total += len(bits)
+    assert total == 2 * (int(top) + 1)
