@@ -48,6 +48,7 @@ SIGNATURES = {
     "fp8_gemm_quant_a": (_i32, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _vp, _i32, _i64, _i64, _i64, _vp, _vp]),
     "fp8_gemm_quant_a_noalloc": (_i32, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _vp, _i32, _i64, _i64, _i64, _vp]),
     "fp8fg_status_string": (ctypes.c_char_p, [_i32]),
+    "fp8fg_check_compute_capability": (_i32, [_i32, _i32]),
     "fp8fg_last_device_status": (_i32, [_vp]),
     "fp8fg_selftest_watchdog": (_i32, [_i64, _vp]),
     "fp8fg_set_wait_limit": (_i32, [_i64]),

@@ -54,7 +54,7 @@ int current_device(DeviceInfo** out) {
             cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
             cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
             return kErrCuda;
-        d.supported = (major == 10 && minor == 3);
+        d.supported = fp8fg_check_compute_capability(major, minor) == kOk;
         d.num_sms = sms;
         if (d.supported) {
             void* addr = nullptr;
@@ -262,6 +262,10 @@ int fp8_gemm_grouped(const uint8_t* a, const float* sa, const uint8_t* b, const 
     g.offsets = group_offsets;
     g.G = G;
     return gemm_common(g, stream);
+}
+
+int fp8fg_check_compute_capability(int major, int minor) {
+    return major == 10 && minor == 3 ? kOk : kErrUnsupported;
 }
 
 const char* fp8fg_status_string(int status) {

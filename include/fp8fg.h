@@ -262,6 +262,16 @@ int fp8_gemm_quant_a_noalloc(const void *a_bf16, uint8_t *q_a, float *s_a,
 const char *fp8fg_status_string(int status);
 
 /*
+ * fp8fg_check_compute_capability -- the device rule every entry point
+ * applies to the current device before any launch: FP8FG_OK for compute
+ * capability 10.3 (sm_103: the kernels use tcgen05, TMEM and TMA as
+ * compiled for that architecture only), FP8FG_ERR_UNSUPPORTED_DEVICE for
+ * any other; there is no fallback path.  Pure function of its arguments
+ * (touches no device), so the rule can be checked without such a device.
+ */
+int fp8fg_check_compute_capability(int major, int minor);
+
+/*
  * fp8fg_last_device_status -- read and clear the device status word of the
  * current device (an asynchronous error recorded by a kernel: a bounded
  * wait that ran out, or invalid grouped offsets).  The word is one per

@@ -24,7 +24,7 @@ def test_header_declares_the_entry_points():
     names = _declared_functions()
     for n in ["fp8_quant_act_1x128", "fp8_quant_act_dual", "fp8_quant_w_128x128", "fp8_gemm_blockscaled", "fp8_gemm_grouped",
               "fp8fg_status_string", "fp8fg_last_device_status", "fp8fg_selftest_watchdog",
-              "fp8fg_set_wait_limit"]:
+              "fp8fg_set_wait_limit", "fp8fg_check_compute_capability"]:
         assert n in names
 
 
@@ -42,6 +42,17 @@ def test_status_strings(cuda_lib_path):
                        (5, "TIMEOUT"), (6, "TEARDOWN"), (7, "TOO_LARGE")]:
         assert word in b.status_string(code)
     assert "unknown" in b.status_string(99)
+
+
+def test_compute_capability_rule(cuda_lib_path):
+    """The device rule every entry point applies before a launch: sm_103
+    (10.3) only, with no fallback for any other architecture.  Checked on the
+    rule itself, so no such device is needed."""
+    from fp8_fine_grained_act_gb300 import binding as b
+    lib = b.load()
+    assert lib.fp8fg_check_compute_capability(10, 3) == b.FP8FG_OK
+    for major, minor in [(10, 0), (10, 1), (10, 4), (9, 0), (8, 9), (11, 0), (12, 0), (12, 1), (0, 0), (-1, 3)]:
+        assert lib.fp8fg_check_compute_capability(major, minor) == b.FP8FG_ERR_UNSUPPORTED_DEVICE
 
 
 def test_noalloc_rejects_oversize_on_the_host(cuda_lib_path):
