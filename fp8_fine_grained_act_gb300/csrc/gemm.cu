@@ -106,8 +106,9 @@ constexpr uint64_t kHandoffLimitNs = 3 * kMaxWaitLimitNs;
 constexpr uint64_t kTeardownLimitNs = 10000000ull;
 
 // Shared memory.  kRowB = 1 (B scales per row of B) also keeps a ring of
-// the chunks' B scales and A scales.  (Three operand stages measured faster than four on
-// the Fprop shape: the fourth leaves almost no L1 for the scale loads.)
+// the chunks' B scales and A scales, staged by warp 3 (run_scales).  (Three
+// operand stages measured faster than four on the Fprop shape: the fourth
+// leaves almost no L1 for the scale loads.)
 template <int kRowB>
 struct __align__(1024) Smem {
     static constexpr int kStages = BN == 256 ? 3 : 4;
@@ -449,7 +450,7 @@ struct TileScales {
     bool active;
     const float* sbp;       // block B scales of this warp's 128 columns, chunk 0
     const float* sap;       // A scale of this thread's row, chunk 0
-    float sb_cur, sb_nxt;   // block B scales: lane l holds chunk l / 32 + l
+    float sb_cur, sb_nxt;   // block B scales of chunks 32 w + l (lane l): the current window w, the next
     float q[4];             // A scales of chunks 0 .. 3 (a chunk past the tile's last repeats the last)
 };
 
@@ -608,8 +609,8 @@ FP8FG_DEV void run_epilogue(Smem<0>& sm, uint32_t tmem_base, const Params& p, co
 // Per-row B scales (Wgrad: both operands scaled per 128-token chunk, one
 // scale per output row i and one per output column j): every partial sum
 // takes its own product sa_i * sb_j, two FP32 operations per sum.  The
-// chunk's B and A scales arrive in shared memory with the chunk (the
-// producer's bulk copies).  TMEM is read with the 16x256b shape, so that a
+// chunk's B and A scales come from the shared ring warp 3 fills in a
+// permuted order (run_scales).  TMEM is read with the 16x256b shape, so that a
 // thread holds 4 rows x 32 columns of its warp's 32 x 128 block and needs 32
 // B scales and 4 A scales per chunk: a thread that held one whole row would
 // need all 128 of its columns' B scales every chunk.  Shared-memory loads
