@@ -19,8 +19,7 @@
 // warpgroup 0 gives registers to the promotion warpgroups with setmaxnreg):
 //   warp 0      TMA producer: A tile [128 x 128 B] and B tile [256 x 128 B]
 //               per K chunk into a 3-stage shared-memory ring (128-byte
-//               swizzle) and, for per-row B scales, the chunk's B scales
-//               into a ring of their own; everything completes on mbarriers;
+//               swizzle), completing on mbarriers;
 //   warp 1      MMA issuer (lane 0 issues, the warp waits): before reusing a
 //               TMEM buffer it takes the buffer back from the promotion
 //               warps on a named barrier (bar.sync), learns from warp 2 on
@@ -41,16 +40,19 @@
 //   warp 2      operand watcher: waits for each chunk's "full" mbarrier and
 //               meets the MMA warp on a named barrier (bar.red.or carries a
 //               failed wait);
-//   warp 3      idle;
+//   warp 3      per-row B scales only: stages each chunk's B and A scales
+//               from global memory into a shared ring, in an order that lets
+//               each promotion thread read its own with 16-byte loads;
 //   warps 4-11  promotion: wait for the buffer, tcgen05.ld 8 x 16 columns
 //               (the next load in flight while the previous 16 columns are
 //               scaled and added with packed FP32 FMAs), hand the buffer back
 //               (bar.arrive), and after the tile's last chunk write the
-//               128 x 256 outputs through shared memory with TMA stores.  The
-//               A scales come straight from global memory, three chunks
-//               ahead, into registers (a tile's first ones during the previous
-//               tile's stores); block B scales come 32 chunks per load, one
-//               per lane, and are broadcast by shuffles.
+//               128 x 256 outputs through shared memory with TMA stores.  With
+//               block B scales the A scales come straight from global memory,
+//               four chunks ahead, into registers (a tile's first ones during
+//               the previous tile's stores), and the B scales 32 chunks per
+//               load, one per lane, broadcast by shuffles; per-row B scales
+//               come from warp 3's ring.
 // The MMA of chunk c+1 runs while the promotion warps fold chunk c.
 #include <cuda.h>
 #include <cuda_runtime.h>
