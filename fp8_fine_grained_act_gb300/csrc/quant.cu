@@ -414,45 +414,26 @@ __global__ void __launch_bounds__(512, 2) quant_w_kernel(const float4* __restric
 #pragma unroll
             for (int k = 0; k < 8; ++k) code[k] = quant_quad<kM>(v[k].x, v[k].y, v[k].z, v[k].w, gs);
         });
-        // 16-byte code stores: lane quad m (lanes 4m .. 4m+3) holds columns
-        // 16m .. 16m+15 of the rows 4 wid + k (+ 64 h) as a 4 x 4 block of
-        // words (row k, lane i); a transpose through three quad shuffles
-        // leaves lane 4m + i with the 16 codes of row k = i
+        // 16-byte code stores: the warp's 8 rows of codes (4 bytes per lane
+        // and row) go through its own 1 KB of the shared tile (rows 8 wid ..
+        // 8 wid + 7 of tq, one 128-byte row each: conflict-free word stores),
+        // then each lane reads 16 bytes of one row back and stores them
         {
-            const int i = lane & 3;
+            uint32_t* stage = &tq[8 * wid][0];
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const uint32_t* a = code + 4 * h;
-                auto pick = [&](int idx) {   // a[idx] by selects (no local memory)
-                    uint32_t v = a[0];
-                    v = idx == 1 ? a[1] : v;
-                    v = idx == 2 ? a[2] : v;
-                    v = idx == 3 ? a[3] : v;
-                    return v;
-                };
-                // x[d] = word (row i, lane i ^ d): lane i sends its word of the partner's row
-                uint32_t x[4];
-                x[0] = pick(i);
+            for (int k = 0; k < 8; ++k) stage[32 * k + lane] = code[k];
+            __syncwarp();
 #pragma unroll
-                for (int d = 1; d < 4; ++d) x[d] = __shfl_xor_sync(0xffffffffu, pick(i ^ d), d);
-                auto pickx = [&](int d) {
-                    uint32_t v = x[0];
-                    v = d == 1 ? x[1] : v;
-                    v = d == 2 ? x[2] : v;
-                    v = d == 3 ? x[3] : v;
-                    return v;
-                };
-                uint4 o;
-                o.x = pickx(i);
-                o.y = pickx(i ^ 1);
-                o.z = pickx(i ^ 2);
-                o.w = pickx(i ^ 3);
-                const int64_t r = r0 + 64 * h + 4 * wid + i;
-                __stcs(reinterpret_cast<uint4*>(q) + (r * cols + c0) / 16 + (lane >> 2), o);
+            for (int u = 0; u < 2; ++u) {
+                const int k = 4 * u + (lane >> 3);   // staged row: code[k] of every lane
+                const uint4 o = *reinterpret_cast<const uint4*>(&stage[32 * k + 4 * (lane & 7)]);
+                const int64_t r = r0 + 64 * (k >> 2) + 4 * wid + (k & 3);
+                __stcs(reinterpret_cast<uint4*>(q) + (r * cols + c0) / 16 + (lane & 7), o);
             }
         }
         if (t == 0) scales[br * nbc + bc] = s;
         if (q_t != nullptr) {
+            __syncthreads();   // every warp has read its staged codes back out of tq
             // transpose each 4x4 byte block: word k holds row k, byte u = column u
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
