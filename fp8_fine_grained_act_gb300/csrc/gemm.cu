@@ -40,9 +40,10 @@
 //   warp 2      operand watcher: waits for each chunk's "full" mbarrier and
 //               meets the MMA warp on a named barrier (bar.red.or carries a
 //               failed wait);
-//   warp 3      per-row B scales only: stages each chunk's B and A scales
-//               from global memory into a shared ring, in an order that lets
-//               each promotion thread read its own with 16-byte loads;
+//   warp 3      per-row B scales only: copies each chunk's B and A scales
+//               from global memory by cp.async into a shared ring of slots
+//               of 4 chunks, in an order that lets each promotion thread
+//               read its own with 16-byte loads;
 //   warps 4-11  promotion: wait for the buffer, tcgen05.ld 8 x 16 columns
 //               (the next load in flight while the previous 16 columns are
 //               scaled and added with packed FP32 FMAs), hand the buffer back
@@ -107,6 +108,13 @@ constexpr uint64_t kHandoffLimitNs = 3 * kMaxWaitLimitNs;
 // far above a copy's latency; running out records kErrTeardown.
 constexpr uint64_t kTeardownLimitNs = 10000000ull;
 
+// Per-row B scales: chunks per slot of the scale ring.  The promotion warps
+// wait for a slot and release it once per group of chunks: a build without
+// the per-chunk wait, warp vote and arrival (not a correct kernel) ran the
+// Wgrad GEMM 17% faster; groups of 4 recover 4% (groups of 2 were slower,
+// groups of 8 do not fit in shared memory).
+constexpr int kScaleGroup = 4;
+
 // Shared memory.  kRowB = 1 (B scales per row of B) also keeps a ring of
 // the chunks' B scales and A scales, staged by warp 3 (run_scales).  (Three
 // operand stages measured faster than four on the Fprop shape: the fourth
@@ -114,12 +122,12 @@ constexpr uint64_t kTeardownLimitNs = 10000000ull;
 template <int kRowB>
 struct __align__(1024) Smem {
     static constexpr int kStages = BN == 256 ? 3 : 4;
-    static constexpr int kSlots = kRowB ? 8 : 1;
+    static constexpr int kSlots = kRowB ? 3 : 1;   // per-row scale ring: slots of kScaleGroup chunks
     uint8_t a[kStages][A_BYTES];
     uint8_t b[kStages][B_BYTES];
     uint8_t out[EPI_WARPS][32 * 128];   // per promotion warp: 32 rows x 128 B, 128-byte swizzle
-    float sb[kSlots][BN];
-    float sa[kRowB ? kSlots : 1][kRowB ? BM : 4];
+    float sb[kSlots][kRowB ? kScaleGroup : 1][BN];
+    float sa[kSlots][kRowB ? kScaleGroup : 1][kRowB ? BM : 4];
     uint64_t full[kStages];
     uint64_t done[kDone];
     uint64_t sfull[kSlots];
@@ -288,63 +296,72 @@ FP8FG_DEV void run_producer(Smem<kRowB>& sm, const CUtensorMap* tmap_a, const CU
 }
 
 // ---------------------------------------------- per-row scale stager ---
-// Per-row B scales only; warp 3.  For every chunk, in the MMA warp's order:
-// load the chunk's B scales of the tile's 256 columns and A scales of its
-// 128 rows from global memory, wait until the promotion warps have released
-// the ring slot, and store the scales into it permuted so that a promotion
-// thread (run_epilogue_rowb) finds its 4 A scales in one 16-byte run and the
-// B scales of each 32 of its columns in two.  Every lane then arrives on the
-// slot's "full" barrier (count 32).  Layouts of a slot:
+// Per-row B scales only; warp 3.  The ring's slots hold kScaleGroup chunks
+// each.  For every group of chunks, in the MMA warp's order: wait until the
+// promotion warps have released the slot, then copy each chunk's B scales
+// of the tile's 256 columns and A scales of its 128 rows from global memory
+// straight into the slot by cp.async, permuted so that a promotion thread
+// (run_epilogue_rowb) finds its 4 A scales in one 16-byte run and the B
+// scales of each 32 of its columns in two.  Every lane then makes the
+// slot's "full" barrier (count 32) take its arrival once its own copies have
+// landed, so the warp neither holds the scales in registers nor waits for
+// the loads.  Layouts of a chunk in a slot:
 //   B: position 128 h + 32 s + 16 p + 4 q + 2 b + e holds column
 //      128 h + 32 s + 8 (2 p + b) + 2 q + e of the tile;
 //   A: position 32 u + 4 r + k holds row 32 u + r + 8 k.
-// Lane l stores positions 4 l .. 4 l + 3 of A and of each half h of B, so
-// each store instruction writes 512 contiguous bytes.  The scales are not
-// copied by TMA because the permutation has 8-byte granularity; doing it
-// here keeps the promotion warps' shared loads (which compete with the
-// tensor core's operand reads) at 9 per chunk instead of 20.
+// Lane l fills positions 4 l .. 4 l + 3 of A and of each half h of B.  The
+// scales are not copied by TMA because the permutation has 8-byte
+// granularity; doing it here keeps the promotion warps' shared loads (which
+// compete with the tensor core's operand reads) at 9 per chunk instead of
+// 20, and one slot per group keeps their ring handshakes at one per group.
 FP8FG_DEV void run_scales(Smem<1>& sm, const Params& p, int64_t m_tiles, int64_t n_tiles, int64_t kb, int lane) {
-    constexpr int SL = Smem<1>::kSlots;
+    constexpr int SL = Smem<1>::kSlots, G = kScaleGroup;
     volatile int* abort_flag = &sm.abort_flag;
     const int64_t num_tiles = m_tiles * n_tiles;
     // this lane's B columns cb, cb + 1, cb + 8, cb + 9 (and + 128), A rows ra + 8 k
     const int cb = 32 * (lane >> 3) + 16 * ((lane >> 2) & 1) + 2 * (lane & 3);
     const int ra = 32 * (lane >> 3) + (lane & 7);
-    uint32_t g = 0;
+    uint32_t gq = 0;   // groups of G chunks staged
     for (int64_t t = blockIdx.x; t < num_tiles; t += gridDim.x) {
         int64_t m0, n0;
         tile_origin(t, m_tiles, n_tiles, p.m_fastest, m0, n0);
         const bool hi = n0 + 128 < p.N;   // the tile's second 128 columns exist (N is a multiple of 128)
-        for (int64_t c = 0; c < kb; ++c, ++g) {
-            const uint32_t sl = g % SL, sph = (g / SL) & 1;
-            // the loads go out before the wait for the slot
-            const float* sbr = p.sb + c * p.N + n0 + cb;
-            const float* sar = p.sa + c * p.M + m0 + ra;
-            const float2 b0 = __ldg(reinterpret_cast<const float2*>(sbr));
-            const float2 b1 = __ldg(reinterpret_cast<const float2*>(sbr + 8));
-            float2 b2 = make_float2(0.0f, 0.0f), b3 = make_float2(0.0f, 0.0f);
-            if (hi) {
-                b2 = __ldg(reinterpret_cast<const float2*>(sbr + 128));
-                b3 = __ldg(reinterpret_cast<const float2*>(sbr + 136));
-            }
-            float a[4];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) a[k] = __ldg(sar + 8 * k);
+        for (int64_t c0 = 0; c0 < kb; c0 += G, ++gq) {
+            const uint32_t sl = gq % SL, sph = (gq / SL) & 1;
             bool ok = true;
             if (lane == 0)
                 ok = mbar_wait_bounded(smem_u32(&sm.sempty[sl]), sph ^ 1, abort_flag, p.status, p.limit_ns,
                                        kErrTimeout);
-            if (!__shfl_sync(0xffffffffu, ok, 0)) return;
-            const uint32_t sb_s = smem_u32(sm.sb[sl]) + 16 * lane, sa_s = smem_u32(sm.sa[sl]) + 16 * lane;
-            st_shared_v4(sb_s, __float_as_uint(b0.x), __float_as_uint(b0.y), __float_as_uint(b1.x),
-                         __float_as_uint(b1.y));
-            st_shared_v4(sb_s + 512, __float_as_uint(b2.x), __float_as_uint(b2.y), __float_as_uint(b3.x),
-                         __float_as_uint(b3.y));
-            st_shared_v4(sa_s, __float_as_uint(a[0]), __float_as_uint(a[1]), __float_as_uint(a[2]),
-                         __float_as_uint(a[3]));
-            mbar_arrive(smem_u32(&sm.sfull[sl]));
+            if (!__shfl_sync(0xffffffffu, ok, 0)) {
+                cp_async_wait_all();   // no copy of this warp outlives it
+                return;
+            }
+            // the group's scales go straight from global memory into their
+            // permuted places by cp.async (no registers held, no wait here);
+            // the slot's "full" barrier counts this lane's arrival once its
+            // copies have landed.  Columns past N and chunks past the tile's
+            // last are not copied (never read).
+#pragma unroll
+            for (int q = 0; q < G; ++q) {
+                const int64_t c = c0 + q;
+                if (c < kb) {
+                    const float* sbr = p.sb + c * p.N + n0 + cb;
+                    const float* sar = p.sa + c * p.M + m0 + ra;
+                    const uint32_t sb_s = smem_u32(sm.sb[sl][q]) + 16 * lane, sa_s = smem_u32(sm.sa[sl][q]) + 16 * lane;
+                    cp_async_8(sb_s, sbr);
+                    cp_async_8(sb_s + 8, sbr + 8);
+                    if (hi) {
+                        cp_async_8(sb_s + 512, sbr + 128);
+                        cp_async_8(sb_s + 520, sbr + 136);
+                    }
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) cp_async_4(sa_s + 4 * k, sar + 8 * k);
+                }
+            }
+            cp_async_mbar_arrive_noinc(smem_u32(&sm.sfull[sl]));
         }
     }
+    cp_async_wait_all();
 }
 
 // ------------------------------------------------------- operand watcher ---
@@ -628,7 +645,7 @@ FP8FG_DEV void run_epilogue(Smem<0>& sm, uint32_t tmem_base, const Params& p, co
 // acc[16 j + 4 bb + 2 rr + e].
 FP8FG_DEV void run_epilogue_rowb(Smem<1>& sm, uint32_t tmem_base, const Params& p, const CUtensorMap* tmap_d,
                                  int64_t m_tiles, int64_t n_tiles, int64_t kb, int warp, int lane) {
-    constexpr int SL = Smem<1>::kSlots;
+    constexpr int SL = Smem<1>::kSlots, G = kScaleGroup;
     volatile int* abort_flag = &sm.abort_flag;
     const int quad = warp & 3;          // TMEM lanes this warp may read: 32*quad .. 32*quad+31
     const int half = (warp - 4) >> 2;   // columns ECOLS*half .. ECOLS*half+ECOLS-1 of the tile
@@ -636,6 +653,7 @@ FP8FG_DEV void run_epilogue_rowb(Smem<1>& sm, uint32_t tmem_base, const Params& 
     const uint32_t ob = smem_u32(sm.out[warp - 4]);
     const int64_t num_tiles = m_tiles * n_tiles;
     uint32_t g = 0;
+    uint32_t gq = 0;   // scale groups (kScaleGroup chunks, one ring slot each) consumed
     bool dead = false;   // after a failed wait: no work, but still one hand-back per chunk
     bool timed_out = false;
     for (int64_t t = blockIdx.x; t < num_tiles; t += gridDim.x) {
@@ -648,7 +666,8 @@ FP8FG_DEV void run_epilogue_rowb(Smem<1>& sm, uint32_t tmem_base, const Params& 
         for (int j = 0; j < ECOLS; ++j) acc[j] = 0.0f;
         for (int64_t c = 0; c < kb; ++c) {
             const uint32_t buf = g % NBUF;
-            const uint32_t sl = g % SL, sph = (g / SL) & 1;
+            const uint32_t sl = gq % SL, sph = (gq / SL) & 1;
+            const int cq = static_cast<int>(c % G);   // chunk within the slot's group
             // (the waits as in run_epilogue)
             bool ok = wait_plain(smem_u32(&sm.done[g & (kDone - 1)]), (g / kDone) & 1,
                                  timed_out ? 1000000ull : kHandoffLimitNs);
@@ -660,7 +679,7 @@ FP8FG_DEV void run_epilogue_rowb(Smem<1>& sm, uint32_t tmem_base, const Params& 
                 dead = true;
                 timed_out = true;
             }
-            if (!dead) {
+            if (!dead && cq == 0) {   // the group's scales have been staged
                 ok = mbar_wait_bounded(smem_u32(&sm.sfull[sl]), sph, abort_flag, p.status, p.limit_ns, kErrTimeout);
                 if (!__all_sync(0xffffffffu, ok)) dead = true;
             }
@@ -670,8 +689,8 @@ FP8FG_DEV void run_epilogue_rowb(Smem<1>& sm, uint32_t tmem_base, const Params& 
                 // the slot's permuted layouts (run_scales): A rows 8k + g4 of
                 // this warp's 32 at 4 g4 + k, B columns 8 bb + 2 q + e of each
                 // 32 at 16 (bb / 2) + 4 q + 2 (bb % 2) + e
-                const uint32_t sbp = smem_u32(sm.sb[sl] + ECOLS * half + 4 * q);
-                const uint4 sa4 = ld_shared_v4(smem_u32(sm.sa[sl] + quad * 32 + 4 * g4));
+                const uint32_t sbp = smem_u32(sm.sb[sl][cq] + ECOLS * half + 4 * q);
+                const uint4 sa4 = ld_shared_v4(smem_u32(sm.sa[sl][cq] + quad * 32 + 4 * g4));
                 // A scales of rows 8k + g4: (rh, rr) = (k / 2, k % 2)
                 const float sav[4] = {__uint_as_float(sa4.x), __uint_as_float(sa4.y), __uint_as_float(sa4.z),
                                       __uint_as_float(sa4.w)};
@@ -715,8 +734,11 @@ FP8FG_DEV void run_epilogue_rowb(Smem<1>& sm, uint32_t tmem_base, const Params& 
             // the buffer goes back only after the loaded registers are consumed
             tc_fence_before();
             named_arrive<kRelThreads>(1 + static_cast<int>(buf));
-            __syncwarp();   // every lane's scale loads from the slot are done
-            if (!dead && lane == 0) mbar_arrive(smem_u32(&sm.sempty[sl]));
+            if (cq == G - 1 || c == kb - 1) {   // the group's last chunk: the slot goes back
+                __syncwarp();   // every lane's scale loads from the slot are done
+                if (!dead && lane == 0) mbar_arrive(smem_u32(&sm.sempty[sl]));
+                ++gq;
+            }
             ++g;
         }
         if (!active || dead) continue;
