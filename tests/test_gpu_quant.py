@@ -39,7 +39,7 @@ def test_act_rows_small(gpu_device, shape):
     _act_parity(synth.activations_random_outliers(rng, *shape), 0, gpu_device)
 
 
-@pytest.mark.parametrize("shape", [(128, 64), (256, 8), (384, 200), (512, 1000)])
+@pytest.mark.parametrize("shape", [(128, 64), (256, 8), (384, 200), (512, 1000), (640, 384)])
 def test_act_cols_small(gpu_device, shape):
     rng = np.random.default_rng(200 + shape[1])
     _act_parity(synth.gradients_token_outliers(rng, *shape), 1, gpu_device)
