@@ -109,7 +109,7 @@ int fp8_quant_act_dual(const void* x_bf16, int64_t rows, int64_t cols, uint8_t* 
     DeviceInfo* d = nullptr;
     int st = current_device(&d);
     if (st != kOk) return st;
-    return from_cuda(launch_quant_act_dual(x_bf16, rows, cols, q_row, s_row, q_col_t, s_col, stream));
+    return from_cuda(launch_quant_act_dual(x_bf16, rows, cols, q_row, s_row, q_col_t, s_col, d->num_sms, stream));
 }
 
 int fp8_quant_w_128x128(const float* w, int64_t rows, int64_t cols, uint8_t* q, uint8_t* q_t, float* scales,

@@ -27,7 +27,7 @@ cudaError_t launch_quant_act_rows(const void* x, int64_t rows, int64_t cols, uin
 cudaError_t launch_quant_act_cols(const void* x, int64_t rows, int64_t cols, uint8_t* q, float* scales, int num_sms,
                                   cudaStream_t stream);
 cudaError_t launch_quant_act_dual(const void* x, int64_t rows, int64_t cols, uint8_t* q_row, float* s_row,
-                                  uint8_t* q_col_t, float* s_col, cudaStream_t stream);
+                                  uint8_t* q_col_t, float* s_col, int num_sms, cudaStream_t stream);
 cudaError_t launch_quant_w(const float* w, int64_t rows, int64_t cols, uint8_t* q, uint8_t* q_t, float* scales,
                            int num_sms, cudaStream_t stream);
 

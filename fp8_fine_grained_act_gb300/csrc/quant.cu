@@ -290,6 +290,128 @@ __global__ void __launch_bounds__(256, 4) quant_act_dual_kernel(const uint4* __r
     }
 }
 
+// ------------------------------------- 1 x 128 and 128 x 1, staged tile ----
+// The same outputs as quant_act_dual_kernel, for large tensors (at least
+// kDualStagedTilesPerSm tiles per SM: X[8192,7168] 49.1 against 51.1 us
+// back to back, while on X[4096,7168] the register kernel's four CTAs per SM
+// give fuller rounds of tiles, 26.4 against 27.2 us).  One CTA per
+// 128 x 128 tile of X, 256 threads, 5 CTAs per SM.  The tile is
+// copied into shared memory with cp.async (rows of 64 words + 4 pad words;
+// no registers held while the copies are in flight, so an SM keeps 160 KB
+// of loads in flight), and both passes read it there.  Row pass: a lane quad
+// owns one row's 1x128 group in each of two rounds (rows q and q + 64 for
+// quad q); lane j takes the group's 16-byte chunks 2j, 2j+1, 2j+8, 2j+9, so
+// that its 32 codes form two 16-byte runs of the output row (16-byte
+// stores) and the group's amax, division and reciprocal are shared by 32
+// elements per lane (the pad puts the two rows of a quarter-warp's 16-byte
+// loads on disjoint banks).  Column pass: thread t takes the channel pair
+// t % 64 over 32 tokens (t / 64), a warp reading 32 consecutive words of one
+// row; the 4 partial maxima meet in shared memory, and each thread writes
+// 2 x 16 codes per channel into q_col_t[cols, rows].  The arithmetic is the
+// same as the single-axis kernels', so both outputs equal theirs bit for bit.
+constexpr int kDualStagedTilesPerSm = 16;
+
+__global__ void __launch_bounds__(256, 5) quant_act_dual_staged_kernel(const uint4* __restrict__ x, int64_t rows,
+                                                                       int64_t cols, uint4* __restrict__ q_row,
+                                                                       float* __restrict__ s_row,
+                                                                       uint8_t* __restrict__ q_col_t,
+                                                                       float* __restrict__ s_col) {
+    __shared__ __align__(16) uint32_t tile[kGroup][kTileWords];
+    __shared__ float part[4][kGroup];
+    const int t = threadIdx.x;
+    const int64_t tb = blockIdx.x, cb = blockIdx.y;
+    const int64_t r0 = tb * kGroup, c0 = cb * kGroup;
+    {
+        const int l16 = t & 15, hw = t >> 4;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int r = hw + 16 * u;
+            cp_async_16(smem_u32(&tile[r][4 * l16]), x + ((r0 + r) * cols + c0) / 8 + l16);
+        }
+        cp_async_wait_all();
+        __syncthreads();
+    }
+    {
+        const int j = t & 3;     // lane of the quad
+        const int rq = t >> 2;   // quad: rows rq and rq + 64 of the tile
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int64_t r = r0 + rq + 64 * u;
+            uint4 v[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                v[k] = *reinterpret_cast<const uint4*>(&tile[rq + 64 * u][4 * (2 * j + (k & 1) + 8 * (k >> 1))]);
+            const float amax = quad_amax_bf16(v);
+            const float s = __fdiv_rn(amax, 448.0f);
+            const GroupScale gs(s);
+            uint4 lo, hi;   // codes of chunks 2j, 2j+1 and of chunks 2j+8, 2j+9
+            with_mode(gs, [&](auto md) {
+                constexpr int kM = decltype(md)::value;
+                lo.x = quant_quad_bf16<kM>(v[0].x, v[0].y, gs);
+                lo.y = quant_quad_bf16<kM>(v[0].z, v[0].w, gs);
+                lo.z = quant_quad_bf16<kM>(v[1].x, v[1].y, gs);
+                lo.w = quant_quad_bf16<kM>(v[1].z, v[1].w, gs);
+                hi.x = quant_quad_bf16<kM>(v[2].x, v[2].y, gs);
+                hi.y = quant_quad_bf16<kM>(v[2].z, v[2].w, gs);
+                hi.z = quant_quad_bf16<kM>(v[3].x, v[3].y, gs);
+                hi.w = quant_quad_bf16<kM>(v[3].z, v[3].w, gs);
+            });
+            uint4* dst = q_row + (r * cols + c0) / 16 + j;
+            __stcs(dst, lo);
+            __stcs(dst + 4, hi);
+            if (j == 0) s_row[cb * rows + r] = s;
+        }
+    }
+    const int cp = t & 63;   // channel pair: channels 2cp, 2cp+1 of the tile
+    const int rs = t >> 6;   // token segment: tokens 32rs .. 32rs+31
+    uint32_t m2 = 0;         // both channels' maxima as 16-bit patterns
+#pragma unroll
+    for (int r = 0; r < 32; ++r) m2 = __vmaxu2(m2, tile[32 * rs + r][cp] & 0x7FFF7FFFu);
+    part[rs][2 * cp] = __uint_as_float(m2 << 16);
+    part[rs][2 * cp + 1] = __uint_as_float(m2 & 0xFFFF0000u);
+    __syncthreads();
+    float a0 = part[0][2 * cp], a1 = part[0][2 * cp + 1];
+#pragma unroll
+    for (int k = 1; k < 4; ++k) {
+        a0 = fmaxf(a0, part[k][2 * cp]);
+        a1 = fmaxf(a1, part[k][2 * cp + 1]);
+    }
+    const float s0 = __fdiv_rn(a0, 448.0f), s1 = __fdiv_rn(a1, 448.0f);
+    const GroupScale g0(s0), g1(s1);
+    const int64_t ch0 = c0 + 2 * cp;
+    uint4* dst0 = reinterpret_cast<uint4*>(q_col_t + ch0 * rows + r0 + 32 * rs);
+    uint4* dst1 = reinterpret_cast<uint4*>(q_col_t + (ch0 + 1) * rows + r0 + 32 * rs);
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        uint32_t wk[16];
+#pragma unroll
+        for (int r = 0; r < 16; ++r) wk[r] = tile[32 * rs + 16 * k + r][cp];
+        // channel 2cp: the low halves of four consecutive tokens' words
+        with_mode(g0, [&](auto md) {
+            constexpr int kM = decltype(md)::value;
+            uint4 o;
+            o.x = quant_quad<kM>(bf16_lo(wk[0]), bf16_lo(wk[1]), bf16_lo(wk[2]), bf16_lo(wk[3]), g0);
+            o.y = quant_quad<kM>(bf16_lo(wk[4]), bf16_lo(wk[5]), bf16_lo(wk[6]), bf16_lo(wk[7]), g0);
+            o.z = quant_quad<kM>(bf16_lo(wk[8]), bf16_lo(wk[9]), bf16_lo(wk[10]), bf16_lo(wk[11]), g0);
+            o.w = quant_quad<kM>(bf16_lo(wk[12]), bf16_lo(wk[13]), bf16_lo(wk[14]), bf16_lo(wk[15]), g0);
+            __stcs(dst0 + k, o);
+        });
+        with_mode(g1, [&](auto md) {
+            constexpr int kM = decltype(md)::value;
+            uint4 o;
+            o.x = quant_quad<kM>(bf16_hi(wk[0]), bf16_hi(wk[1]), bf16_hi(wk[2]), bf16_hi(wk[3]), g1);
+            o.y = quant_quad<kM>(bf16_hi(wk[4]), bf16_hi(wk[5]), bf16_hi(wk[6]), bf16_hi(wk[7]), g1);
+            o.z = quant_quad<kM>(bf16_hi(wk[8]), bf16_hi(wk[9]), bf16_hi(wk[10]), bf16_hi(wk[11]), g1);
+            o.w = quant_quad<kM>(bf16_hi(wk[12]), bf16_hi(wk[13]), bf16_hi(wk[14]), bf16_hi(wk[15]), g1);
+            __stcs(dst1 + k, o);
+        });
+    }
+    if (rs == 0) {
+        s_col[tb * cols + ch0] = s0;
+        s_col[tb * cols + ch0 + 1] = s1;
+    }
+}
+
 // ------------------------------------------------------------ 128 x 1 ----
 // The 128x1 quantizer alone when cols is a multiple of 128: one CTA per
 // 128 x 128 tile, 256 threads, 5 CTAs per SM.  The tile (32 KB) is copied
@@ -502,10 +624,16 @@ cudaError_t launch_quant_act_cols(const void* x, int64_t rows, int64_t cols, uin
 }
 
 cudaError_t launch_quant_act_dual(const void* x, int64_t rows, int64_t cols, uint8_t* q_row, float* s_row,
-                                  uint8_t* q_col_t, float* s_col, cudaStream_t stream) {
+                                  uint8_t* q_col_t, float* s_col, int num_sms, cudaStream_t stream) {
     const dim3 grid(static_cast<unsigned>(rows / kGroup), static_cast<unsigned>(cols / kGroup));
-    quant_act_dual_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint4*>(x), rows, cols,
-                                                          reinterpret_cast<uint4*>(q_row), s_row, q_col_t, s_col);
+    const int64_t tiles = (rows / kGroup) * (cols / kGroup);
+    if (tiles >= static_cast<int64_t>(kDualStagedTilesPerSm) * num_sms)
+        quant_act_dual_staged_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint4*>(x), rows, cols,
+                                                                reinterpret_cast<uint4*>(q_row), s_row, q_col_t,
+                                                                s_col);
+    else
+        quant_act_dual_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint4*>(x), rows, cols,
+                                                         reinterpret_cast<uint4*>(q_row), s_row, q_col_t, s_col);
     return cudaPeekAtLastError();
 }
 

@@ -210,6 +210,18 @@ def test_dual_zero_and_tiny_groups(gpu_device):
     _dual_parity(synth.f32_to_bf16_bits(x), gpu_device)
 
 
+def test_dual_zero_and_tiny_groups_large(gpu_device):
+    """The same special groups in a tensor large enough (3584 tiles) for the
+    staged-tile kernel, spread over several tiles."""
+    x = np.zeros((8192, 7168), np.float32)
+    x[5, 3] = -2.0
+    x[130:140, 200] = np.float32(2.0 ** -133)
+    x[200, 128:256] = -0.0
+    x[4000:4128, 5000] = np.float32(448.0)
+    x[8191, 7040:7168] = np.float32(-(2.0 ** -140))
+    _dual_parity(synth.f32_to_bf16_bits(x), gpu_device)
+
+
 def test_dual_full_wgrad_x(gpu_device):
     """X[8192,7168] of the Wgrad workload: the fused kernel against the
     oracle on both axes, and against the two single-axis kernels."""
