@@ -142,23 +142,26 @@ static int gemm_common(const GemmArgs& a, cudaStream_t stream) {
 // Shape rules shared by the dense and grouped GEMMs.  TMA addresses rows of
 // up to 2^32 elements per dimension; the limits below keep every index and
 // byte count far inside int64 and the tensor-map ranges.
-static int check_gemm_shape(int64_t M, int64_t N, int64_t K, int out_dtype) {
+// ragged_m: M need not be a multiple of 128 (the last row tile is partial).
+static int check_gemm_shape(int64_t M, int64_t N, int64_t K, int out_dtype, bool ragged_m = false) {
     if (M < 0 || N < 0 || K < 0) return kErrInvalidArg;
-    if (M % 128 != 0 || N % 128 != 0 || K % 128 != 0) return kErrInvalidArg;
+    if ((!ragged_m && M % 128 != 0) || N % 128 != 0 || K % 128 != 0) return kErrInvalidArg;
     if (out_dtype != FP8FG_OUT_F32 && out_dtype != FP8FG_OUT_BF16) return kErrInvalidArg;
     const int64_t lim = int64_t(1) << 31;
     if (M > lim || N > lim || K > lim) return kErrInvalidArg;
     // output tiles of 128 x 256 are numbered with 32-bit integers
-    if ((M / 128) * ((N + 255) / 256) >= lim) return kErrInvalidArg;
+    if (((M + 127) / 128) * ((N + 255) / 256) >= lim) return kErrInvalidArg;
     return kOk;
 }
 
 int fp8_gemm_blockscaled(const uint8_t* a, const float* sa, const uint8_t* b, const float* sb, int bscale,
                          int64_t sb_stride_n, int64_t sb_stride_k, void* d, int out_dtype, int64_t M, int64_t N,
                          int64_t K, cudaStream_t stream) {
-    int st = check_gemm_shape(M, N, K, out_dtype);
-    if (st != kOk) return st;
     if (bscale != FP8FG_BSCALE_BLOCK128 && bscale != FP8FG_BSCALE_ROW) return kErrInvalidArg;
+    // block B scales (Fprop, Dgrad: M = tokens) take any M; per-row B scales
+    // (Wgrad: M = output channels) need whole row tiles
+    int st = check_gemm_shape(M, N, K, out_dtype, bscale == FP8FG_BSCALE_BLOCK128);
+    if (st != kOk) return st;
     if (bscale == FP8FG_BSCALE_BLOCK128 && (sb_stride_n < 0 || sb_stride_k < 0)) return kErrInvalidArg;
     if (M == 0 || N == 0) return kOk;
     if (!d) return kErrInvalidArg;

@@ -486,7 +486,9 @@ FP8FG_DEV TileScales load_tile_scales(int64_t t, const Params& p, int64_t m_tile
     ts.sbp = p.sb + e * p.sb_group_stride + (ts.col0 / 128) * p.sb_stride_n;
     if (ts.active && lane < kb) ts.sb_cur = __ldg(ts.sbp + lane * p.sb_stride_k);
     if (ts.active && lane + 32 < kb) ts.sb_nxt = __ldg(ts.sbp + (lane + 32) * p.sb_stride_k);
-    ts.sap = p.sa + ts.m0 + row;
+    // rows past M (a partial last row tile) read row M - 1's scales: their
+    // partial sums are zero (the A box reads zeros there) and never stored
+    ts.sap = p.sa + min(ts.m0 + row, p.M - 1);
     // (indices clamped to the last chunk instead of a select on the loaded
     // value: a select would make the thread wait for the load to return)
 #pragma unroll
@@ -580,7 +582,9 @@ FP8FG_DEV void run_epilogue(Smem<0>& sm, uint32_t tmem_base, const Params& p, co
         }
         if (t + gridDim.x < num_tiles)
             nts = load_tile_scales(t + gridDim.x, p, m_tiles, n_tiles, kb, half, row, lane);
-        if (!active || dead) continue;
+        // (a warp whose 32 rows all lie past M, in a partial last row tile,
+        // stores nothing; a store box that crosses M is clipped by TMA)
+        if (!active || dead || m0 + quad * 32 >= p.M) continue;
         // 32 rows x 128 columns of this warp -> shared memory (row = lane,
         // 16-byte chunk k of each 128-byte row at k ^ (row & 7): the 128-byte
         // swizzle of the output map) -> one TMA store per 128 bytes of row;
@@ -967,7 +971,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     extern __shared__ uint8_t smem_raw[];
     S& sm = *reinterpret_cast<S*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t m_tiles = p.M / BM, n_tiles = (p.N + BN - 1) / BN, kb = p.K / BK;
+    const int64_t m_tiles = (p.M + BM - 1) / BM, n_tiles = (p.N + BN - 1) / BN, kb = p.K / BK;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S::kStages; ++s) mbar_init(smem_u32(&sm.full[s]), 1);
@@ -1175,7 +1179,7 @@ int launch_gemm(const GemmArgs& a, int num_sms, int* status_word, cudaStream_t s
     p.qa = reinterpret_cast<uint2*>(const_cast<uint8_t*>(a.a));
     p.sa_out = const_cast<float*>(a.sa);
     p.band_flags = a.band_flags;
-    const int64_t tiles = (a.M / BM) * ((a.N + BN - 1) / BN);
+    const int64_t tiles = ((a.M + BM - 1) / BM) * ((a.N + BN - 1) / BN);
     const int64_t grid = tiles < num_sms ? tiles : num_sms;
     if (grid <= 0) return kOk;
     // the kernel counts a CTA's K chunks (over all its tiles) in 32 bits

@@ -156,10 +156,13 @@ int fp8_quant_w_128x128(const float *w, int64_t rows, int64_t cols,
  *     sb_stride_n and sb_stride_k are ignored;
  *   d[M, N]: float32 (out_dtype FP8FG_OUT_F32) or bfloat16 rounded to
  *     nearest even (FP8FG_OUT_BF16).
- * Requires M % 128 == 0, N % 128 == 0, K % 128 == 0 (tokens are padded to
- * 128 by the caller); a, b and d 16-byte aligned; sa and sb 4-byte aligned
- * for block scales, both 16-byte aligned for per-row B scales (the kernel
- * reads B scales in 8-byte pairs there); sb strides >= 0.
+ * Requires N % 128 == 0 and K % 128 == 0; with per-row B scales also
+ * M % 128 == 0 (Wgrad: M = output channels, K = tokens, padded to 128 by
+ * the caller), while block B scales take any M >= 0 (Fprop, Dgrad:
+ * M = tokens; the last 128-row tile is then partial: its missing rows read
+ * as zero codes and are not written); a, b and d 16-byte aligned; sa and sb
+ * 4-byte aligned for block scales, both 16-byte aligned for per-row B
+ * scales (the kernel reads B scales in 8-byte pairs there); sb strides >= 0.
  * K == 0 writes zeros.  M == 0 or N == 0 is a no-op.
  * Accuracy (tested): |d - o| <= 2^-16 * sum_k |a~ b~| for FP32 output, plus
  * one BF16 spacing of o for BF16 output, o being the exact sum of the

@@ -130,7 +130,10 @@ def test_gemm_argument_checks(lib):
         return f(v["a"], v["sa"], v["b"], v["sb"], v["bscale"], v["sn"], v["sk"], v["d"], v["od"],
                  v["M"], v["N"], v["K"], None)
 
-    assert call(M=100) == 1 and call(N=200) == 1 and call(K=130) == 1
+    assert call(N=200) == 1 and call(K=130) == 1
+    assert call(M=100, bscale=1) == 1                      # per-row B scales: whole row tiles only
+    if not _has_gpu():
+        assert call(M=100) in NOPROBE                      # block B scales take any M
     assert call(M=-128) == 1
     assert call(od=7) == 1 and call(bscale=3) == 1
     assert call(sn=-1) == 1

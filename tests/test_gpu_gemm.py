@@ -7,7 +7,8 @@ sees exactly the oracle's inputs.  Pass: |gpu - o| <= 2^-16 * sum|a~ b~|,
 plus one BF16 spacing of o for BF16 output.
 
 Cases: the tiny Fprop in FP32 and BF16; medium shapes spanning several
-tiles with a ragged N tile (N = 640 is 2.5 tiles of 256); Dgrad through the
+tiles with a ragged N tile (N = 640 is 2.5 tiles of 256); token counts
+that are not a multiple of 128 (Fprop and Dgrad); Dgrad through the
 transposed weight copy and swapped scale strides; Wgrad with per-row B
 scales; an exact integer case (bit-exact); K = 0; the full-size Fprop,
 Dgrad and Wgrad workloads on sampled outputs; and the accumulation probe
@@ -66,6 +67,41 @@ def test_fprop_medium(gpu_device, M, N, K):
         _check_operands(ops, (qx, sx, qw, sw))
         o, m = oracle.gemm(qx, sx, qw, sw)
         assert_gemm_close(host(y), o, m, ODT[out_dtype], f"fprop {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 256, 128), (200, 384, 256), (1000, 640, 384), (290, 128, 640)])
+def test_fprop_ragged_m(gpu_device, M, N, K):
+    """Token counts that are not a multiple of 128: the last 128-row tile
+    is partial (single token, one row past a tile, several tiles plus a
+    tail, and a warp-sized remainder); the rows past M must stay untouched."""
+    d = synth.fprop_linear(seed=7 * M + N + K, M=M, N=N, K=K)
+    qx, sx = oracle.quant_act(d["x"])
+    qw, sw = oracle.quant_w(d["w"])
+    o, m = oracle.gemm(qx, sx, qw, sw)
+    for out_dtype in (F32, BF16):
+        gx, gsx = fb.fp8_quant_act_1x128(dev_bf16(d["x"], gpu_device))
+        gw, gsw = fb.fp8_quant_w_128x128(dev(d["w"], gpu_device))
+        _check_operands((gx, gsx, gw, gsw), (qx, sx, qw, sw))
+        # the output is a view of a taller buffer whose extra rows hold a sentinel
+        dt = torch.float32 if out_dtype == F32 else torch.bfloat16
+        big = torch.full((M + 160, N), 7.0, dtype=dt, device=gpu_device)
+        y = fb.fp8_gemm_blockscaled(gx, gsx, gw, gsw, out_dtype=out_dtype, d=big[:M])
+        torch.cuda.synchronize()
+        assert_gemm_close(host(y), o, m, ODT[out_dtype], f"fprop ragged {M}x{N}x{K}")
+        assert bool((big[M:] == 7.0).all()), "rows past M were written"
+
+
+def test_dgrad_ragged_m(gpu_device):
+    d = synth.dgrad(seed=9, M=333, N=640, K=384)           # dY[333,384], W[384,640], dX[333,640]
+    qdy, sdy = fb.fp8_quant_act_1x128(dev_bf16(d["dy"], gpu_device))
+    qw, qwt, sw = fb.fp8_quant_w_128x128(dev(d["w"], gpu_device), transposed=True)
+    nw = d["w"].shape[1] // 128
+    dx = fb.fp8_gemm_blockscaled(qdy, sdy, qwt, sw, sb_strides=(1, nw), out_dtype=BF16)
+    torch.cuda.synchronize()
+    qdy_o, sdy_o = oracle.quant_act(d["dy"])
+    qw_o, sw_o, qwt_o = oracle.quant_w(d["w"], transposed=True)
+    o, m = oracle.gemm(qdy_o, sdy_o, qwt_o, sw_o, sb_strides=(1, nw))
+    assert_gemm_close(host(dx), o, m, "bf16", "dgrad ragged")
 
 
 def test_dgrad_medium(gpu_device):
