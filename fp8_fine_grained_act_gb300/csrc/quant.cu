@@ -506,10 +506,10 @@ __global__ void __launch_bounds__(512, 2) quant_w_kernel(const float4* __restric
     __shared__ uint32_t tq[kGroup][kGroup / 4];
     const int t = threadIdx.x, lane = t & 31, wid = t >> 5;
     const int64_t nbr = rows / kGroup, nbc = cols / kGroup;
-    for (int64_t blk = blockIdx.x; blk < nbr * nbc; blk += gridDim.x) {
-        const int64_t br = blk / nbc, bc = blk - br * nbc;
-        const int64_t r0 = br * kGroup, c0 = bc * kGroup;
-        float4 v[8];
+    // this thread's 32 values of block `b`: rows 4 wid + k and 64 + 4 wid + k, columns 4 lane .. 4 lane + 3
+    float4 v[8];
+    auto load_block = [&](int64_t b) {
+        const int64_t r0 = (b / nbc) * kGroup, c0 = (b % nbc) * kGroup;
 #pragma unroll
         for (int h = 0; h < 2; ++h)
 #pragma unroll
@@ -517,6 +517,11 @@ __global__ void __launch_bounds__(512, 2) quant_w_kernel(const float4* __restric
                 const int64_t r = r0 + 64 * h + 4 * wid + k;
                 v[4 * h + k] = __ldcs(w + (r * cols + c0) / 4 + lane);
             }
+    };
+    if (blockIdx.x < nbr * nbc) load_block(blockIdx.x);
+    for (int64_t blk = blockIdx.x; blk < nbr * nbc; blk += gridDim.x) {
+        const int64_t br = blk / nbc, bc = blk - br * nbc;
+        const int64_t r0 = br * kGroup, c0 = bc * kGroup;
         float amax = 0.0f;
 #pragma unroll
         for (int k = 0; k < 8; ++k)
@@ -536,6 +541,9 @@ __global__ void __launch_bounds__(512, 2) quant_w_kernel(const float4* __restric
 #pragma unroll
             for (int k = 0; k < 8; ++k) code[k] = quant_quad<kM>(v[k].x, v[k].y, v[k].z, v[k].w, gs);
         });
+        // the next block's loads go out now (v is free): their latency
+        // overlaps this block's stores and barriers
+        if (blk + gridDim.x < nbr * nbc) load_block(blk + gridDim.x);
         // 16-byte code stores: the warp's 8 rows of codes (4 bytes per lane
         // and row) go through its own 1 KB of the shared tile (rows 8 wid ..
         // 8 wid + 7 of tq, one 128-byte row each: conflict-free word stores),
