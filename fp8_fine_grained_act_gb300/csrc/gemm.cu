@@ -111,8 +111,8 @@ constexpr uint64_t kTeardownLimitNs = 10000000ull;
 // Per-row B scales: chunks per slot of the scale ring.  The promotion warps
 // wait for a slot and release it once per group of chunks: a build without
 // the per-chunk wait, warp vote and arrival (not a correct kernel) ran the
-// Wgrad GEMM 17% faster; groups of 4 recover 4% (groups of 2 were slower,
-// groups of 8 do not fit in shared memory).
+// Wgrad GEMM 17% faster; groups of 4 recover 4% (groups of 2 were slower;
+// 8 or 16 chunks per slot, with the 196 KB cap below lifted, no faster).
 constexpr int kScaleGroup = 4;
 
 // Shared memory.  kRowB = 1 (B scales per row of B) also keeps a ring of
