@@ -944,7 +944,7 @@ FP8FG_DEV bool p1_quantize(Smem<kRowB>& sm, const Params& p, int64_t units, int6
 // Warp 0 of every CTA: wait until every band's kb tiles are published
 // (acquire), lane l polling bands l, l + 32, ... (in parallel: one polling
 // thread reading the counters one after another took several microseconds
-// more), each lane bounded by the wait limit.  Returns the same verdict in
+// more), each lane bounded by the wait limit.  Returns the same result in
 // every lane; a timeout records FP8FG_ERR_TIMEOUT and the CTA computes
 // nothing.
 FP8FG_DEV bool wait_bands(const Params& p, int64_t m_tiles, int64_t kb, int lane) {
