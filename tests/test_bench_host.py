@@ -70,3 +70,15 @@ def test_single_core_quantizer_timing_restores_threads():
     assert r["cores"] == 1
     assert r["quant_act_1x128"]["GB/s"] > 0 and r["quant_w_128x128"]["GB/s"] > 0
     assert oracle.num_threads() == n0
+
+
+def test_committed_summaries_describe_the_current_gemm_source():
+    """Every committed GEMM summary names the hash of the GEMM source as it
+    stands, so the bench reports its DRAM traffic (a stale summary would
+    make the traffic null)."""
+    prof = os.path.join(os.path.dirname(bench.__file__), "profiles")
+    names = [n for n in os.listdir(prof) if n.startswith(("gemm_", "launches_"))]
+    assert names
+    h = bench.gemm_source_sha()
+    for n in names:
+        assert h in open(os.path.join(prof, n)).read(), f"{n} was taken on another GEMM source"
